@@ -1,0 +1,443 @@
+"""Benchmark of the PillarAttn attention step on one GB300 (or N replicas).
+
+One step = one unified-batch attention step (the fused persistent draft+verify
+launch: paged addressing, verification with the logit/LSE dump, sparse draft
+attention) followed by pillar selection for the verifying requests
+(reconstruction, averaging, Top-K); bucket assignment runs on the host once
+per batch.  Workload: 256 requests with the attention shape of Qwen3-1.7B
+(16 query / 8 KV heads, d = 128), lengths lognormal with mean 13,542 and sd
+7,626 clipped to [512, 40,960] (stand-in for the AIME output lengths of the
+paper's Table 1), k = 8, s = 0.05, 1% of rows per KV head scaled by 4, paged
+KV with page 16.  Per step the step reads about 2.6 GB, far more than L2, so
+no flush is needed between steps.
+
+Prints one JSON line.  --impl reference times the CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "qwen3_1p7b_b256_aime_len"
+METRIC = "fused draft+verify attn: query-tokens/s and KV HBM GB/s vs GB300 peak"
+UNIT = "query-tokens/s"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------------------
+# workload accounting (algorithmic bytes and query tokens of one step)
+# --------------------------------------------------------------------------------------
+def step_accounting(st):
+    wl = st.wl
+    hkv, hq = wl.num_kv_heads, wl.num_q_heads
+    G = hq // hkv
+    L = wl.seq_lens.astype(np.int64)
+    v = st.is_verify
+    steps = st.steps.astype(np.int64)
+    nsel = st.nsel_host.astype(np.int64)
+    row_bytes = hkv * 128 * 2 * 2                              # K and V of one token, all KV heads
+    kv_verify = int((L[v] * row_bytes).sum())
+    kv_draft = int(((nsel[~v] + steps[~v] + 1) * row_bytes).sum())
+    logit_bytes = int((L[v] * hkv * st.k * G * 4).sum())
+    q_rows = int(st.q_off[-1])
+    io_bytes = q_rows * hq * 128 * 2 * 2 + q_rows * hq * 4      # q in, out, lse
+    idx_bytes = int((nsel[~v] * hkv * 4).sum())
+    bt_bytes = int(((L + 15) // 16 * 4).sum())
+    query_tokens = int(st.k * v.sum() + (~v).sum())
+    fused_bytes = kv_verify + kv_draft + logit_bytes + io_bytes + idx_bytes + bt_bytes
+    # selection: read the dump and LSE, write the averages, re-read them for Top-K, write indices
+    sel_bytes = logit_bytes + int((L[v] * hkv * 4).sum()) * 2 + int((nsel_kept(st)[v] * hkv * 4).sum())
+    return dict(kv_bytes=kv_verify + kv_draft, kv_verify=kv_verify, kv_draft=kv_draft, logit_bytes=logit_bytes,
+                fused_bytes=fused_bytes, select_bytes=sel_bytes, query_tokens=query_tokens,
+                n_verify=int(v.sum()), n_draft=int((~v).sum()),
+                fused_flops=int((4 * st.k * hq * 128 * L[v]).sum() + (4 * hq * 128 * (nsel[~v] + steps[~v] + 1)).sum()))
+
+
+def nsel_kept(st):
+    s32 = float(np.float32(st.s))
+    L = st.wl.seq_lens.astype(np.int64)
+    return np.maximum(1, np.minimum(L, np.floor(s32 * L).astype(np.int64)))
+
+
+# --------------------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import torch
+
+    import synth
+    import sparse_self_speculative_gb300 as ss
+    from tests import harness as hz
+
+    torch.cuda.set_device(local)
+    name = args.workload
+    hq, hkv, B, k, s = synth.WORKLOADS[name]
+    seed = 1000 * 3 + rank
+    wl = synth.named_workload(name, seed)
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="setup")
+    acc = step_accounting(st)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st.fused()
+        st.select()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0, "device error word set"
+
+    # ---- device-resident timed region ----
+    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_s1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            ev_f0[i].record(stream)
+            st.fused()
+            ev_f1[i].record(stream)
+            st.select()
+            ev_s1[i].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(stop)
+    fused_ms = [a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)]
+    select_ms = [a.elapsed_time(b) for a, b in zip(ev_f1, ev_s1)]
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+    tokens_all = sum_over_ranks(acc["query_tokens"] * args.steps, world)
+    value = tokens_all / (ms_step * args.steps / 1e3)
+
+    # ---- end to end: host buffers in, results out, every step ----
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_qoff = pin(st.d_q), pin(st.d_q_off)
+    h_seq, h_sel, h_bucket, h_nsel = pin(st.d_seq), pin(st.d_sel), pin(st.d_bucket), pin(st.d_nsel)
+    h_out = torch.empty_like(st.d_out, device="cpu").pin_memory()
+    h_lse = torch.empty_like(st.d_lse, device="cpu").pin_memory()
+    h_idx = torch.empty_like(st.d_idx, device="cpu").pin_memory()
+    ins = [(st.d_q, h_q), (st.d_q_off, h_qoff), (st.d_seq, h_seq), (st.d_sel, h_sel), (st.d_bucket, h_bucket),
+           (st.d_nsel, h_nsel)]
+    outs = [(h_out, st.d_out), (h_lse, st.d_lse), (h_idx, st.d_idx)]
+    h2d = sum(h.numel() * h.element_size() for _, h in ins)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+
+    def e2e_step():
+        for d, h in ins:
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in outs:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    e2e_value = tokens_all / (e2e_ms * args.steps / 1e3)
+
+    peak, peak_kind = _peaks()
+    f_ms = statistics.mean(fused_ms)
+    achieved = acc["fused_bytes"] / (f_ms / 1e3) / 1e9
+    kv_gbs = acc["kv_bytes"] / (f_ms / 1e3) / 1e9
+    gpu_launches = 2 * args.steps
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: batch {B}, Hq/Hkv {hq}/{hkv}, d 128, page 16, k {k}, s {s}, "
+                               f"{acc['n_verify']} verify + {acc['n_draft']} draft requests",
+                   "global_batch": B * world, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (about 2.6 GB read per step)"},
+        "kv_gbs": kv_gbs,
+        "fused_ms": f_ms, "select_ms": statistics.mean(select_ms),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "attn_persistent (fused step)", "peak_kind": peak_kind,
+                     "kv_gbs": kv_gbs, "kv_frac": kv_gbs / peak},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+        "bytes_per_step": {"kv": acc["kv_bytes"], "fused_total": acc["fused_bytes"], "select": acc["select_bytes"]},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(st, seconds=args.cpu_seconds)
+    return result
+
+
+def cpu_baseline(st, seconds: float = 15.0, n_verify: int = 2, n_draft: int = 16):
+    """The oracle as it stands, timed on the host cores over a bounded sample of the
+    same step (the first verifying and drafting requests in batch order, with the
+    pillars the device step uses), repeated until about `seconds` of oracle time."""
+    import oracle
+    from tests import harness as hz
+    wl = st.wl
+    hkv = wl.num_kv_heads
+    sample = []
+    v_ids = [int(r) for r in np.flatnonzero(st.is_verify)][:n_verify]
+    d_ids = [int(r) for r in np.flatnonzero(~st.is_verify)][:n_draft]
+    idx_all = st.d_idx.cpu().numpy()
+    for r in v_ids:
+        L = int(wl.seq_lens[r])
+        kf, vf = st.kv_f64(r, np.arange(L))
+        sample.append(("v", r, st.q_f64(r), kf, vf, None))
+    for r in d_ids:
+        L = int(wl.seq_lens[r])
+        stride = (st.idx_off[r + 1] - st.idx_off[r]) // hkv
+        ns = int(st.nsel_host[r])
+        blk = idx_all[st.idx_off[r]:st.idx_off[r + 1]]
+        pillars = [blk[h * stride: h * stride + ns] for h in range(hkv)]
+        need = np.unique(np.concatenate(pillars + [np.arange(int(st.sel_lens[r]), L)]))
+        kf = np.zeros((L, hkv, 128))
+        vf = np.zeros((L, hkv, 128))
+        kf[need], vf[need] = st.kv_f64(r, need)
+        sample.append(("d", r, st.q_f64(r)[0], kf, vf, pillars))
+    tokens = st.k * len(v_ids) + len(d_ids)
+    passes, t = 0, 0.0
+    while t < seconds or passes == 0:
+        t0 = time.perf_counter()
+        for kind, r, q, kf, vf, pillars in sample:
+            if kind == "v":
+                _, lse, lg = oracle.verify_attention(q, kf, vf, hz.SCALE)
+                S = oracle.average_scores(lg, lse, wl.group)
+                K = oracle.pillar_count(st.s, int(wl.seq_lens[r]))
+                for h in range(hkv):
+                    oracle.top_k_pillars(S[h], K)
+            else:
+                oracle.sparse_draft_attention(q, kf, vf, pillars, int(st.sel_lens[r]), hz.SCALE)
+        t += time.perf_counter() - t0
+        passes += 1
+    return {"value": tokens * passes / t, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{len(v_ids)} verify + {len(d_ids)} draft requests of the step, "
+                      f"{passes} passes in {t:.1f} s (numpy float64 oracle)"}
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# --------------------------------------------------------------------------------------
+def run_reference(args):
+    import oracle
+    import synth
+    from tests import harness as hz
+
+    name = args.workload
+    hq, hkv, B, k, s = synth.WORKLOADS[name]
+    wl = synth.named_workload(name, 1000 * 3)
+    buckets, _ = oracle.assign_buckets(k, [0] * (k + 1), B)
+    L = wl.seq_lens.astype(np.int64)
+    steps = np.array([hz.draft_step(int(b), 0, k) for b in buckets])
+    # bounded sample per step: one verifying request and eight drafting ones (pillars: seeded)
+    v_ids = [int(r) for r in np.flatnonzero(steps < 0)][:1]
+    d_ids = [int(r) for r in np.flatnonzero(steps >= 0)][:8]
+    prepared = []
+    for r in v_ids:
+        kf = oracle.bf16_bits_to_f64(wl.kv_rows("k", r, np.arange(L[r])))
+        vf = oracle.bf16_bits_to_f64(wl.kv_rows("v", r, np.arange(L[r])))
+        prepared.append(("v", r, oracle.bf16_bits_to_f64(wl.q_rows(r, np.arange(k))), kf, vf, None, None))
+    for r in d_ids:
+        sel = int(L[r] - steps[r] - 1)
+        ps = hz.synthetic_pillars(wl.seed, r, hkv, sel, oracle.pillar_count(s, sel))
+        need = np.unique(np.concatenate(ps + [np.arange(sel, L[r])]))
+        kf = np.zeros((L[r], hkv, 128))
+        vf = np.zeros((L[r], hkv, 128))
+        kf[need] = oracle.bf16_bits_to_f64(wl.kv_rows("k", r, need))
+        vf[need] = oracle.bf16_bits_to_f64(wl.kv_rows("v", r, need))
+        prepared.append(("d", r, oracle.bf16_bits_to_f64(wl.q_rows(r, np.arange(1)))[0], kf, vf, ps, sel))
+
+    def step():
+        for kind, r, q, kf, vf, ps, sel in prepared:
+            if kind == "v":
+                _, lse, lg = oracle.verify_attention(q, kf, vf, hz.SCALE)
+                S = oracle.average_scores(lg, lse, hq // hkv)
+                K = oracle.pillar_count(s, int(L[r]))
+                for h in range(hkv):
+                    oracle.top_k_pillars(S[h], K)
+            else:
+                oracle.sparse_draft_attention(q, kf, vf, ps, sel, hz.SCALE)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    tokens = k * len(v_ids) + len(d_ids)
+    value = tokens / dt
+    cores = _blas_threads()
+    sample = f"{len(v_ids)} verify + {len(d_ids)} draft requests of the step (numpy float64 oracle)"
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": name, "global_batch": B, "parallelism": "cpu"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return 0
+    res = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,218 @@
+/*
+ * sspec.h -- C ABI of the GB300 (sm_103a) PillarAttn attention step.
+ *
+ * The method is PillarAttn from "Accelerating Large-Scale Reasoning Model
+ * Inference with Sparse Self-Speculative Decoding" (SparseSpec; MLSys 2026
+ * talk-notes page, sections "PillarAttn: dynamic sparse attention" = paper
+ * Sec. 4.1 / Fig. 7 and "Unified batch scheduler" = paper Sec. 4.2 / Fig. 8):
+ * full verification attention dumps its scores as logits + log-sum-exp, the
+ * scores are reconstructed and averaged over the k draft queries and each GQA
+ * group, Top-K picks the "pillar" tokens, and the next k draft steps attend to
+ * the pillars only.  One persistent launch serves a unified batch in which one
+ * bucket verifies while the other k draft.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers marked "device" are device memory of the current CUDA device;
+ *    "host" pointers are read before the call returns.  The caller owns every
+ *    buffer.  The library never allocates, frees or synchronises; each compute
+ *    call enqueues its kernels on `stream` and returns.
+ *  - bf16 tensors are raw 16-bit bfloat16 bit patterns.  Head dim d = 128 and
+ *    page size 16 are the only supported values (SSPEC_ERR_UNSUPPORTED_SHAPE
+ *    otherwise).
+ *  - Paged KV cache: K and V are separate arrays, each
+ *        bf16 [num_pages][num_kv_heads][16][128]
+ *    so one (page, kv head) block is 4 KiB contiguous.  Token t of request r
+ *    lives in page block_table[r * max_pages_per_req + t / 16], slot t % 16.
+ *  - GQA: G = num_q_heads / num_kv_heads; query head hq reads KV head hq / G.
+ *  - Softmax uses the scaled logit  l = sm_scale * dot(q, k)  and the natural
+ *    log-sum-exp  lse = ln(sum exp(l)).
+ *  - Return value: SSPEC_OK (0) or a negative SSPEC_ERR_* code detected on the
+ *    host, in which case nothing was enqueued.  Errors only the device can see
+ *    (a page or pillar index out of range, inconsistent lengths, a dump range
+ *    or workspace too small for the lengths held in device memory) OR a bit
+ *    into the int32 error word at byte 0 of the workspace (SSPEC_DEVERR_*),
+ *    skip the offending work, and never trap.  The word is sticky: the caller
+ *    reads it when convenient and clears it.
+ *  - Workspace: caller-allocated device memory of at least
+ *    sspec_workspace_size() bytes, ZERO-FILLED BEFORE ITS FIRST USE.  Every
+ *    call leaves the counters it uses back at zero, so a workspace can be
+ *    reused without clearing; it must not be shared by calls that may run
+ *    concurrently (one workspace per stream).
+ */
+#ifndef SSPEC_H_
+#define SSPEC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* sspec_stream_t;
+
+enum {
+  SSPEC_OK = 0,
+  SSPEC_ERR_INVALID_ARG = -1,       /* null pointer, negative size, s outside (0,1], ... */
+  SSPEC_ERR_UNSUPPORTED_SHAPE = -2, /* head_dim != 128, page != 16, too many query rows */
+  SSPEC_ERR_WORKSPACE_TOO_SMALL = -3,
+  SSPEC_ERR_CUDA = -4               /* a CUDA runtime call or launch failed */
+};
+
+/* Bits of the device error word (int32 at byte 0 of the workspace). */
+enum {
+  SSPEC_DEVERR_PAGE_OOB = 1,        /* block-table entry outside [0, num_pages) */
+  SSPEC_DEVERR_INDEX_OOB = 2,       /* pillar index outside [0, sel_len) */
+  SSPEC_DEVERR_LENGTH = 4,          /* seq_len / sel_len / nsel inconsistent or too long */
+  SSPEC_DEVERR_RANGE = 8,           /* logit / index range of a request too small */
+  SSPEC_DEVERR_WORKSPACE = 16       /* workspace too small for the lengths in device memory */
+};
+
+/* Largest batch one call accepts. */
+#define SSPEC_MAX_BATCH 1024
+/* Largest number of query rows per (request, KV head): nq * G for verification. */
+#define SSPEC_MAX_ROWS 64
+
+typedef struct {
+  int32_t num_q_heads;   /* Hq */
+  int32_t num_kv_heads;  /* Hkv, Hq % Hkv == 0 */
+  int32_t head_dim;      /* must be 128 */
+  int32_t page_size;     /* must be 16 */
+  float sm_scale;        /* usually 1/sqrt(128) */
+} sspec_shape;
+
+typedef struct {
+  const void* k_cache;              /* device bf16 [num_pages][Hkv][16][128] */
+  const void* v_cache;              /* device bf16 [num_pages][Hkv][16][128] */
+  const int32_t* block_table;       /* device int32 [batch][max_pages_per_req] */
+  int32_t max_pages_per_req;        /* row stride of block_table; seq_len <= 16 * this */
+  int32_t num_pages;                /* pages in each cache array */
+} sspec_paged_kv;
+
+/*
+ * Bytes of workspace any entry point needs for a call over `batch` requests
+ * whose largest per-request query row count is nq * G (nq = the verify query
+ * count, k) and whose per-request token counts sum to at most
+ * `total_kv_tokens` (verify: seq_len; draft: nsel + seq_len - sel_len).
+ * Host only; returns 0 for invalid arguments.
+ */
+size_t sspec_workspace_size(const sspec_shape* shape, int32_t batch, int32_t nq,
+                            int64_t total_kv_tokens);
+
+/*
+ * Verification attention with the logit / LSE dump
+ * (PillarAttn, "overhead-free identification": the verify stage computes full
+ * attention and a custom kernel writes its scores on the fly as logits and
+ * log-sum-exp; paper Sec. 4.1).
+ *
+ * Each of `batch` requests has nq query rows, the last nq tokens of its
+ * sequence: query j sits at position seq_lens[r] - nq + j and attends to keys
+ * 0 .. seq_lens[r] - nq + j (causal among the verify tokens).
+ *   q         device bf16 [batch][nq][Hq][128]
+ *   seq_lens  device int32 [batch], nq <= seq_len <= 16 * max_pages_per_req
+ *   out       device bf16 [batch][nq][Hq][128]
+ *   lse       device fp32 [batch][nq][Hq]
+ *   logits    device fp32, nullable (no dump).  Request r's dump starts at
+ *             element logit_off[r] and is laid out [Hkv][nq*G][seq_len],
+ *             row j*G+g holding query j of head h*G+g; masked entries are -inf.
+ *             logit_off[r+1] - logit_off[r] must be >= Hkv*nq*G*seq_len.
+ *   logit_off device int64 [batch+1] (ignored when logits is null)
+ */
+int sspec_verify_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
+                      int32_t nq, const void* q, const int32_t* seq_lens, void* out,
+                      float* lse, float* logits, const int64_t* logit_off, void* workspace,
+                      size_t ws_bytes, sspec_stream_t stream);
+
+/*
+ * Pillar selection: reconstruct, average, Top-K
+ * (PillarAttn: the dumped logits and LSE are restored to probabilities and
+ * averaged over the k draft queries and the query heads of each GQA group;
+ * Top-K of the average gives the critical tokens; paper Sec. 4.1).
+ *
+ * For every request r whose logit range logit_off[r] .. logit_off[r+1] is
+ * non-empty (others are skipped, so the dump of a unified batch can be passed
+ * as is), with L = seq_lens[r] and K = max(1, min(L, floor((double)s * L))):
+ *   S[h][t] = (1/(nq*G)) * sum_{j<nq, g<G} exp(logit[h][j*G+g][t] - lse[j][h*G+g])
+ *   idx of head h = the K positions with the largest S[h][.], equal scores
+ *   going to the lower position, written ascending.
+ *   logits, logit_off  as written by sspec_verify_attn / sspec_fused_step;
+ *                      logit_off[r] must be a multiple of nq*G.
+ *   lse        device fp32, row (q_off ? q_off[r] : r*nq) + j of width Hq
+ *   q_off      device int64 [batch+1] or null
+ *   avg_scores device fp32, nullable: S of request r, [Hkv][L], at element
+ *              logit_off[r] / (nq*G).  When null, S lives in the workspace.
+ *   idx        device int32: head h of request r at idx_off[r] + h*stride,
+ *              stride = (idx_off[r+1] - idx_off[r]) / Hkv, which must be >= K.
+ *   nsel       device int32 [batch]: K of each processed request.
+ */
+int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, float s,
+                         const float* logits, const int64_t* logit_off, const float* lse,
+                         const int64_t* q_off, const int32_t* seq_lens, float* avg_scores,
+                         int32_t* idx, const int64_t* idx_off, int32_t* nsel, void* workspace,
+                         size_t ws_bytes, sspec_stream_t stream);
+
+/*
+ * Sparse draft attention over the pillars
+ * (PillarAttn: the draft loads and computes only the critical tokens; the
+ * pattern selected at the last verification is reused for the next k draft
+ * steps; paper Sec. 4.1 / Fig. 7).
+ *
+ * One query per request and head, at position seq_lens[r] - 1.  Head h attends
+ * to its nsel[r] pillar positions (idx, all < sel_lens[r]) followed by every
+ * token appended since selection, positions sel_lens[r] .. seq_lens[r]-1; the
+ * softmax is over that set only.
+ *   q        device bf16 [batch][Hq][128]
+ *   seq_lens, sel_lens  device int32 [batch], 0 <= sel_len < seq_len
+ *   idx, idx_off, nsel  as written by sspec_select_pillars
+ *   out      device bf16 [batch][Hq][128];  lse  device fp32 [batch][Hq]
+ */
+int sspec_sparse_draft_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
+                            const void* q, const int32_t* seq_lens, const int32_t* sel_lens,
+                            const int32_t* idx, const int64_t* idx_off, const int32_t* nsel,
+                            void* out, float* lse, void* workspace, size_t ws_bytes,
+                            sspec_stream_t stream);
+
+/*
+ * One unified-batch attention step in a single persistent launch
+ * (Unified batch scheduler + fused attention kernel: draft sparse attention
+ * and verify full attention of the same batch are dispatched to their own
+ * templates inside one persistent kernel; paper Sec. 4.2, Fig. 8 and Fig. 15).
+ *
+ * Request r verifies (as sspec_verify_attn with nq = k) when
+ * bucket[r] == verify_bucket and otherwise takes one sparse draft step (as
+ * sspec_sparse_draft_attn).  Query, output and LSE rows are ragged:
+ *   q         device bf16 [rows][Hq][128]; request r owns rows q_off[r] ..
+ *             q_off[r+1]-1 (k rows to verify, 1 row to draft)
+ *   q_off     device int64 [batch+1]
+ *   out       device bf16 [rows][Hq][128];  lse  device fp32 [rows][Hq]
+ *   logits / logit_off  dump of the verifying requests (drafts may have
+ *             empty ranges); logits nullable
+ *   sel_lens, idx, idx_off, nsel  read for drafting requests only
+ */
+int sspec_fused_step(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
+                     int32_t k, const int32_t* bucket, int32_t verify_bucket, const void* q,
+                     const int64_t* q_off, const int32_t* seq_lens, const int32_t* sel_lens,
+                     const int32_t* idx, const int64_t* idx_off, const int32_t* nsel, void* out,
+                     float* lse, float* logits, const int64_t* logit_off, void* workspace,
+                     size_t ws_bytes, sspec_stream_t stream);
+
+/*
+ * Greedy least-loaded bucket assignment (Unified batch scheduler: new requests
+ * go to the least-loaded of the k+1 buckets; paper Sec. 4.2, Fig. 8).
+ * Host only.  The load of a bucket is its request count; requests are placed in
+ * index order; ties go to the lower bucket id.
+ *   counts      host int32 [k+1], in: current counts, out: updated counts
+ *   bucket_out  host int32 [n_new]
+ */
+int sspec_assign_buckets(int32_t k, int32_t* counts, int32_t n_new, int32_t* bucket_out);
+
+/* Static English text of an SSPEC_* return code. */
+const char* sspec_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSPEC_H_ */

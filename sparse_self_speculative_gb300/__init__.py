@@ -1,0 +1,184 @@
+"""Python binding of libsspec.so, the GB300 PillarAttn attention step.
+
+Argument marshalling only: every function forwards to the C entry point of the
+same name in ``include/sspec.h`` (tensors become device pointers, the stream is
+the current PyTorch stream unless given).  All computation happens in the CUDA
+kernels of the library; there is no fallback.  If the library has not been
+built, importing the functions raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsspec.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "sspec.h")
+
+SSPEC_OK = 0
+SSPEC_ERR_INVALID_ARG = -1
+SSPEC_ERR_UNSUPPORTED_SHAPE = -2
+SSPEC_ERR_WORKSPACE_TOO_SMALL = -3
+SSPEC_ERR_CUDA = -4
+SSPEC_DEVERR_PAGE_OOB = 1
+SSPEC_DEVERR_INDEX_OOB = 2
+SSPEC_DEVERR_LENGTH = 4
+SSPEC_DEVERR_RANGE = 8
+SSPEC_DEVERR_WORKSPACE = 16
+SSPEC_MAX_BATCH = 1024
+SSPEC_MAX_ROWS = 64
+
+
+class SspecShape(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float)]
+
+
+class SspecPagedKV(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("max_pages_per_req", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32)]
+
+
+class SspecError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} returned {code}: {error_string(code)}")
+        self.code = code
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SIGS = {
+    "sspec_workspace_size": (ctypes.c_size_t, [_P, _I32, _I32, ctypes.c_int64]),
+    "sspec_verify_attn": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "sspec_select_pillars": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P,
+                                            _P, _P, ctypes.c_size_t, _P]),
+    "sspec_sparse_draft_attn": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                               ctypes.c_size_t, _P]),
+    "sspec_fused_step": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P, _P, ctypes.c_size_t, _P]),
+    "sspec_assign_buckets": (ctypes.c_int, [_I32, _P, _I32, _P]),
+    "sspec_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def lib():
+    """The loaded libsspec.so; raises if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built: run __graft_entry__.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/sspec.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(sspec_\w+)\s*\(", text, re.M)))
+
+
+def error_string(code: int) -> str:
+    return lib().sspec_error_string(int(code)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != SSPEC_OK:
+        raise SspecError(fn, rc)
+
+
+def make_shape(num_q_heads: int, num_kv_heads: int, sm_scale: float | None = None) -> SspecShape:
+    return SspecShape(num_q_heads, num_kv_heads, 128, 16, (128 ** -0.5) if sm_scale is None else sm_scale)
+
+
+def make_kv(k_cache, v_cache, block_table) -> SspecPagedKV:
+    kv = SspecPagedKV(_ptr(k_cache), _ptr(v_cache), _ptr(block_table), int(block_table.shape[1]),
+                      int(k_cache.shape[0]))
+    kv._keep = (k_cache, v_cache, block_table)   # the struct holds raw pointers: keep the tensors alive
+    return kv
+
+
+def sspec_workspace_size(shape: SspecShape, batch: int, nq: int, total_kv_tokens: int) -> int:
+    return int(lib().sspec_workspace_size(ctypes.byref(shape), batch, nq, total_kv_tokens))
+
+
+def sspec_verify_attn(shape, kv, batch, nq, q, seq_lens, out, lse, logits, logit_off, workspace,
+                      stream=None):
+    rc = lib().sspec_verify_attn(ctypes.byref(shape), ctypes.byref(kv), batch, nq, _ptr(q), _ptr(seq_lens),
+                                 _ptr(out), _ptr(lse), _ptr(logits), _ptr(logit_off), _ptr(workspace),
+                                 _nbytes(workspace), _stream(stream))
+    _check("sspec_verify_attn", rc)
+
+
+def sspec_select_pillars(shape, batch, nq, s, logits, logit_off, lse, q_off, seq_lens, avg_scores, idx,
+                         idx_off, nsel, workspace, stream=None):
+    rc = lib().sspec_select_pillars(ctypes.byref(shape), batch, nq, float(s), _ptr(logits), _ptr(logit_off),
+                                    _ptr(lse), _ptr(q_off), _ptr(seq_lens), _ptr(avg_scores), _ptr(idx),
+                                    _ptr(idx_off), _ptr(nsel), _ptr(workspace), _nbytes(workspace),
+                                    _stream(stream))
+    _check("sspec_select_pillars", rc)
+
+
+def sspec_sparse_draft_attn(shape, kv, batch, q, seq_lens, sel_lens, idx, idx_off, nsel, out, lse,
+                            workspace, stream=None):
+    rc = lib().sspec_sparse_draft_attn(ctypes.byref(shape), ctypes.byref(kv), batch, _ptr(q), _ptr(seq_lens),
+                                       _ptr(sel_lens), _ptr(idx), _ptr(idx_off), _ptr(nsel), _ptr(out),
+                                       _ptr(lse), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check("sspec_sparse_draft_attn", rc)
+
+
+def sspec_fused_step(shape, kv, batch, k, bucket, verify_bucket, q, q_off, seq_lens, sel_lens, idx, idx_off,
+                     nsel, out, lse, logits, logit_off, workspace, stream=None):
+    rc = lib().sspec_fused_step(ctypes.byref(shape), ctypes.byref(kv), batch, k, _ptr(bucket), verify_bucket,
+                                _ptr(q), _ptr(q_off), _ptr(seq_lens), _ptr(sel_lens), _ptr(idx),
+                                _ptr(idx_off), _ptr(nsel), _ptr(out), _ptr(lse), _ptr(logits),
+                                _ptr(logit_off), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check("sspec_fused_step", rc)
+
+
+def sspec_assign_buckets(k: int, counts, n_new: int):
+    """Host call; ``counts`` is a list of k+1 ints.  Returns (buckets, new counts)."""
+    c = (ctypes.c_int32 * (k + 1))(*[int(x) for x in counts])
+    out = (ctypes.c_int32 * max(1, n_new))()
+    rc = lib().sspec_assign_buckets(k, c, n_new, out)
+    _check("sspec_assign_buckets", rc)
+    return list(out)[:n_new], list(c)
+
+
+def _nbytes(t):
+    if t is None:
+        return 0
+    return t.numel() * t.element_size()
+
+
+__all__ = [
+    "SspecShape", "SspecPagedKV", "SspecError", "lib", "make_shape", "make_kv", "error_string",
+    "sspec_workspace_size", "sspec_verify_attn", "sspec_select_pillars", "sspec_sparse_draft_attn",
+    "sspec_fused_step", "sspec_assign_buckets", "header_functions",
+]

@@ -1,0 +1,554 @@
+// Persistent draft + verify attention for sm_103a.
+//
+// One launch serves a whole batch in which each request either verifies
+// (full causal attention of its nq query rows over every cached token, with
+// the logit dump) or takes one sparse draft step (one query row per head over
+// its pillars plus the tail appended since selection).  This is the fused
+// kernel of SparseSpec's unified batch scheduler (talk notes, section
+// "Unified batch scheduler", paper Sec. 4.2 / Fig. 15) serving PillarAttn
+// (section "PillarAttn", paper Sec. 4.1).
+//
+// Work decomposition: a unit is (request, kv head, chunk of kChunk entries of
+// the request's token list).  Verification lists positions 0..L-1, a draft
+// step its pillars then its tail.  Units are handed out by an atomic counter
+// (no CTA ever waits on another); each unit writes a partial softmax state
+// and the last unit of a (request, head) to arrive merges them.
+//
+// Inside a unit, K/V rows (256 B per token and head) are staged with 16-byte
+// cp.async into an XOR-swizzled shared-memory ring, and both products run on
+// the tensor cores with mma.m16n8k16 (bf16 in, fp32 accumulate): the query
+// rows of one KV head (nq*G for verification, G for a draft) form the M side,
+// padded to 16.  The softmax is the usual running-max form; all warps share
+// the per-row maximum of each tile through shared memory.
+#include <cfloat>
+#include <cmath>
+
+#include "device_common.cuh"
+#include "internal.cuh"
+
+namespace sspec {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kRowBytes = kHeadDim * 2;  // one token row of one head: 256 B
+
+struct Req {
+  bool verify;
+  int L;          // tokens in the cache
+  int T;          // length of the token list
+  int rows;       // query rows of one kv head
+  long long qbase;
+  int sel_len;
+  int nsel;
+  long long idx_base;
+  long long idx_stride;
+  long long loff;
+};
+
+__device__ __forceinline__ bool is_verify(const AttnParams& p, int r) {
+  return p.mode == kAllVerify || (p.mode == kByBucket && p.bucket[r] == p.verify_bucket);
+}
+
+// Reads request r's description; returns false (and reports, when asked) if its
+// lengths are inconsistent, in which case the request is skipped.
+__device__ bool load_req(const AttnParams& p, int r, Req& q, bool report) {
+  q.verify = is_verify(p, r);
+  q.L = p.seq_lens[r];
+  const int cap = p.max_pages * kPage;
+  int bad = 0;
+  if (q.verify) {
+    q.rows = p.nq * p.group;
+    q.T = q.L;
+    q.qbase = p.q_off ? p.q_off[r] : (long long)r * p.nq;
+    q.sel_len = q.nsel = 0;
+    q.idx_base = q.idx_stride = 0;
+    q.loff = p.logits ? p.logit_off[r] : 0;
+    if (q.L < p.nq || q.L > cap) bad |= SSPEC_DEVERR_LENGTH;
+    if (p.q_off && p.q_off[r + 1] - p.q_off[r] < p.nq) bad |= SSPEC_DEVERR_LENGTH;
+    if (p.logits && !bad &&
+        p.logit_off[r + 1] - p.logit_off[r] < (long long)p.hkv * q.rows * q.L)
+      bad |= SSPEC_DEVERR_RANGE;
+  } else {
+    q.rows = p.group;
+    q.qbase = p.q_off ? p.q_off[r] : (long long)r;
+    q.sel_len = p.sel_lens[r];
+    q.nsel = p.nsel[r];
+    q.loff = 0;
+    if (q.sel_len < 0 || q.L <= q.sel_len || q.L > cap || q.nsel < 0 || q.nsel > q.sel_len)
+      bad |= SSPEC_DEVERR_LENGTH;
+    if (p.q_off && p.q_off[r + 1] - p.q_off[r] < 1) bad |= SSPEC_DEVERR_LENGTH;
+    q.idx_base = p.idx_off[r];
+    q.idx_stride = (p.idx_off[r + 1] - p.idx_off[r]) / p.hkv;
+    if (!bad && q.nsel > q.idx_stride) bad |= SSPEC_DEVERR_RANGE;
+    q.T = q.nsel + (q.L - q.sel_len);
+  }
+  if (bad && report) atomicOr(p.err, bad);
+  return bad == 0;
+}
+
+template <int MT>
+struct Smem {
+  static constexpr int kKV = kStages * kTile * kRowBytes;   // one of K or V ring
+  static constexpr int kQ = MT * 16 * kRowBytes;
+  static constexpr int kP = MT * 16 * kTile * 2;
+  static constexpr int kRowIds = kChunk * 4;
+  static constexpr int kRed = kAttnWarps * MT * 16 * 4;
+  static constexpr int off_k = 0;
+  static constexpr int off_v = off_k + kKV;
+  static constexpr int off_q = off_v + kKV;
+  static constexpr int off_p = off_q + kQ;
+  static constexpr int off_rows = off_p + kP;
+  static constexpr int off_rmax = off_rows + kRowIds;
+  static constexpr int off_rl = off_rmax + kRed;
+  static constexpr int off_prefix = off_rl + kRed;
+  static size_t bytes(int batch) { return off_prefix + size_t(batch + 1) * 4; }
+};
+
+// byte offset of 16-byte chunk `ch` of row `row` in a 256-byte-row swizzled tile
+__device__ __forceinline__ uint32_t swz256(int row, int ch) {
+  return uint32_t(row * kRowBytes + ((ch ^ (row & 7)) << 4));
+}
+// same for the 128-byte rows of the probability tile
+__device__ __forceinline__ uint32_t swz128(int row, int ch) {
+  return uint32_t(row * (kTile * 2) + ((ch ^ (row & 7)) << 4));
+}
+
+template <int MT>
+__device__ void merge_partials(const AttnParams& p, const Req& q, int h, long long u0, int nch) {
+  const size_t ustride = size_t(p.rows_max) * (kHeadDim + 2);
+  const float* base = p.partials + size_t(u0) * ustride;
+  const int G = p.group;
+  for (int e = threadIdx.x; e < q.rows * (kHeadDim / 2); e += kAttnThreads) {
+    const int row = e / (kHeadDim / 2);
+    const int d = (e % (kHeadDim / 2)) * 2;
+    float M = -INFINITY;
+    for (int c = 0; c < nch; ++c)
+      M = fmaxf(M, __ldcg(base + c * ustride + size_t(p.rows_max) * kHeadDim + row));
+    float lsum = 0.f, o0 = 0.f, o1 = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const float* pc = base + c * ustride;
+      const float w = exp2f(__ldcg(pc + size_t(p.rows_max) * kHeadDim + row) - M);
+      lsum += w * __ldcg(pc + size_t(p.rows_max) * (kHeadDim + 1) + row);
+      const float2 ov = __ldcg(reinterpret_cast<const float2*>(pc + row * kHeadDim + d));
+      o0 += w * ov.x;
+      o1 += w * ov.y;
+    }
+    const float inv = 1.f / lsum;
+    const long long orow = q.verify ? q.qbase + row / G : q.qbase;
+    const int hq = h * G + (q.verify ? row % G : row);
+    *reinterpret_cast<uint32_t*>(p.out + (size_t(orow) * p.hq + hq) * kHeadDim + d) =
+        pack_bf16x2(o0 * inv, o1 * inv);
+    if (d == 0) p.lse[size_t(orow) * p.hq + hq] = (M + log2f(lsum)) * kLn2;
+  }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams p) {
+  using S = Smem<MT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sK = smem_addr(smem + S::off_k);
+  const uint32_t sV = smem_addr(smem + S::off_v);
+  const uint32_t sQ = smem_addr(smem + S::off_q);
+  const uint32_t sP = smem_addr(smem + S::off_p);
+  int32_t* s_row = reinterpret_cast<int32_t*>(smem + S::off_rows);
+  float* red_max = reinterpret_cast<float*>(smem + S::off_rmax);
+  float* red_l = reinterpret_cast<float*>(smem + S::off_rl);
+  int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + S::off_prefix);
+  __shared__ int s_warp[kAttnWarps];
+  __shared__ int s_misc[2];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g8 = lane >> 2, tq = lane & 3;
+  const int B = p.batch;
+
+  // ---- per-request unit counts and their prefix (each CTA computes its own copy) ----
+  {
+    const int per = (B + kAttnThreads - 1) / kAttnThreads;
+    int sum = 0;
+    for (int i = 0; i < per; ++i) {
+      const int r = tid * per + i;
+      int units = 0;
+      if (r < B) {
+        Req q;
+        if (load_req(p, r, q, blockIdx.x == 0)) units = ((q.T + kChunk - 1) / kChunk) * p.hkv;
+        s_prefix[r + 1] = units;
+      }
+      sum += units;
+    }
+    int total;
+    int run = block_exclusive_scan<kAttnThreads>(sum, s_warp, &total);
+    for (int i = 0; i < per; ++i) {
+      const int r = tid * per + i;
+      if (r < B) {
+        run += s_prefix[r + 1];
+        s_prefix[r + 1] = run;
+      }
+    }
+    if (tid == 0) s_prefix[0] = 0;
+    __syncthreads();
+  }
+  long long total = s_prefix[B];
+  if (total > p.unit_capacity) {
+    if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, SSPEC_DEVERR_WORKSPACE);
+    total = 0;
+  }
+
+  for (;;) {
+    __syncthreads();
+    if (tid == 0) s_misc[0] = int(atomicAdd(p.q_next, 1u));
+    __syncthreads();
+    const long long u = s_misc[0];
+    if (u >= total) break;
+
+    // ---- decode the unit ----
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    const int r = lo;
+    Req q;
+    load_req(p, r, q, false);
+    const int nch = (s_prefix[r + 1] - s_prefix[r]) / p.hkv;
+    const int local = int(u - s_prefix[r]);
+    const int h = local / nch, c = local % nch;
+    const int tok0 = c * kChunk;
+    const int ntok = min(q.T - tok0, kChunk);
+    const int mt_used = (q.rows + 15) >> 4;
+    const int G = p.group;
+
+    // ---- 1. row ids (page * Hkv + h) * 16 + slot of every entry of the chunk ----
+    for (int i = tid; i < ntok; i += kAttnThreads) {
+      const int e = tok0 + i;
+      int pos;
+      int bad = 0;
+      if (q.verify) {
+        pos = e;
+      } else if (e < q.nsel) {
+        pos = p.idx[q.idx_base + h * q.idx_stride + e];
+        if (pos < 0 || pos >= q.sel_len) bad = SSPEC_DEVERR_INDEX_OOB;
+      } else {
+        pos = q.sel_len + (e - q.nsel);
+      }
+      int rid = -1;
+      if (!bad) {
+        const int pg = p.block_table[size_t(r) * p.max_pages + (pos >> 4)];
+        if (pg < 0 || pg >= p.num_pages) bad = SSPEC_DEVERR_PAGE_OOB;
+        else rid = (pg * p.hkv + h) * kPage + (pos & (kPage - 1));
+      }
+      if (bad) atomicOr(p.err, bad);
+      s_row[i] = rid;
+    }
+
+    // ---- 2. query rows of this kv head into shared memory (zero padded) ----
+    for (int e = tid; e < MT * 16 * 16; e += kAttnThreads) {
+      const int row = e >> 4, ch = e & 15;
+      const bool valid = row < q.rows;
+      const uint16_t* src = p.q;
+      if (valid) {
+        const long long qrow = q.verify ? q.qbase + row / G : q.qbase;
+        const int hq = h * G + (q.verify ? row % G : row);
+        src = p.q + (size_t(qrow) * p.hq + hq) * kHeadDim + ch * 8;
+      }
+      cp_async16(sQ + swz256(row, ch), src, valid);
+    }
+    cp_async_commit();
+    __syncthreads();
+
+    const int ntiles = (ntok + kTile - 1) / kTile;
+    auto load_tile = [&](int t, int st) {
+      const uint32_t kb = sK + st * kTile * kRowBytes;
+      const uint32_t vb = sV + st * kTile * kRowBytes;
+#pragma unroll
+      for (int m = 0; m < (kTile * 16) / kAttnThreads; ++m) {
+        const int e = tid + m * kAttnThreads;
+        const int row = e >> 4, ch = e & 15;
+        const int i = t * kTile + row;
+        const int rid = (i < ntok) ? s_row[i] : -1;
+        const size_t off = size_t(rid < 0 ? 0 : rid) * kHeadDim + ch * 8;
+        cp_async16(kb + swz256(row, ch), p.k_cache + off, rid >= 0);
+        cp_async16(vb + swz256(row, ch), p.v_cache + off, rid >= 0);
+      }
+    };
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+      if (s < ntiles) load_tile(s, s);
+      cp_async_commit();
+    }
+
+    float m_run[MT][2], l_run[MT][2];
+    float o[MT][4][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) { m_run[mt][hh] = -INFINITY; l_run[mt][hh] = 0.f; }
+#pragma unroll
+      for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][n][i] = 0.f;
+    }
+    const bool dump = q.verify && p.logits != nullptr;
+    const int vis_base = q.L - p.nq;  // query j sees positions <= vis_base + j
+
+    for (int t = 0; t < ntiles; ++t) {
+      cp_async_wait<kStages - 2>();
+      __syncthreads();
+      {
+        const int tn = t + kStages - 1;
+        if (tn < ntiles) load_tile(tn, tn % kStages);
+        cp_async_commit();
+      }
+      const int st = t % kStages;
+      const uint32_t kb = sK + st * kTile * kRowBytes;
+      const uint32_t vb = sV + st * kTile * kRowBytes;
+
+      // ---- S = Q K^T for this warp's 16 tokens ----
+      float sacc[MT][2][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sacc[mt][nt][i] = 0.f;
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {
+        uint32_t bk[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          ldsm_x4(kb + swz256(warp * 16 + nt * 8 + (lane & 7), kp * 4 + (lane >> 3)), bk[nt]);
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int ks = kp * 2 + e2;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            if (mt < mt_used) {
+              uint32_t a[4];
+              ldsm_x4(sQ + swz256(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, ks * 2 + (lane >> 4)), a);
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(sacc[mt][nt], a, bk[nt][2 * e2], bk[nt][2 * e2 + 1]);
+            }
+          }
+        }
+      }
+
+      // ---- mask, dump, per-row tile maximum ----
+      float rmax[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) { rmax[mt][0] = -INFINITY; rmax[mt][1] = -INFINITY; }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii) {
+          const int tok = warp * 16 + nt * 8 + tq * 2 + ii;
+          const int i = t * kTile + tok;
+          const bool valid = i < ntok && s_row[i] >= 0;
+          const int pos = tok0 + i;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int row = mt * 16 + g8 + hh * 8;
+              const float x = sacc[mt][nt][hh * 2 + ii];
+              bool vis = valid;
+              if (q.verify) vis = vis && pos <= vis_base + row / G;
+              if (dump && mt < mt_used && row < q.rows && i < ntok)
+                p.logits[q.loff + (size_t(h) * q.rows + row) * q.L + pos] = vis ? x * p.sm_scale : -INFINITY;
+              const float s2 = vis ? x * p.scale_log2 : -INFINITY;
+              sacc[mt][nt][hh * 2 + ii] = s2;
+              rmax[mt][hh] = fmaxf(rmax[mt][hh], s2);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v = rmax[mt][hh];
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+          if (tq == 0) red_max[warp * MT * 16 + mt * 16 + g8 + hh * 8] = v;
+        }
+      __syncthreads();
+
+      // ---- new running max, probabilities, rescale ----
+      float alpha[MT][2], muse[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = mt * 16 + g8 + hh * 8;
+          float tmax = red_max[row];
+#pragma unroll
+          for (int w = 1; w < kAttnWarps; ++w) tmax = fmaxf(tmax, red_max[w * MT * 16 + row]);
+          const float m_new = fmaxf(m_run[mt][hh], tmax);
+          muse[mt][hh] = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha[mt][hh] = exp2f(m_run[mt][hh] - muse[mt][hh]);
+          m_run[mt][hh] = m_new;
+        }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        float ls[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float pv = exp2f(sacc[mt][nt][i] - muse[mt][i >> 1]);
+            sacc[mt][nt][i] = pv;
+            ls[i >> 1] += pv;
+          }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) l_run[mt][hh] = l_run[mt][hh] * alpha[mt][hh] + ls[hh];
+        if (mt < mt_used) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int row = mt * 16 + g8 + hh * 8;
+              st_shared_u32(sP + swz128(row, warp * 2 + nt) + tq * 4,
+                            pack_bf16x2(sacc[mt][nt][hh * 2], sacc[mt][nt][hh * 2 + 1]));
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[mt][n][i] *= alpha[mt][i >> 1];
+      }
+      __syncthreads();
+
+      // ---- O += P V for this warp's 32 output dims ----
+#pragma unroll
+      for (int kt = 0; kt < kTile / 16; ++kt) {
+        uint32_t bv[2][4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+          ldsm_x4_trans(vb + swz256(kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, warp * 4 + half * 2 + (lane >> 4)),
+                        bv[half]);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          if (mt < mt_used) {
+            uint32_t a[4];
+            ldsm_x4(sP + swz128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kt * 2 + (lane >> 4)), a);
+#pragma unroll
+            for (int n = 0; n < 4; ++n) mma_bf16_16816(o[mt][n], a, bv[n >> 1][(n & 1) * 2], bv[n >> 1][(n & 1) * 2 + 1]);
+          }
+        }
+      }
+    }
+
+    // ---- epilogue: full row sums ----
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float v = l_run[mt][hh];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (tq == 0) red_l[warp * MT * 16 + mt * 16 + g8 + hh * 8] = v;
+      }
+    __syncthreads();
+    float ltot[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = mt * 16 + g8 + hh * 8;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) s += red_l[w * MT * 16 + row];
+        ltot[mt][hh] = s;
+      }
+
+    if (nch == 1) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = mt * 16 + g8 + hh * 8;
+          if (mt < mt_used && row < q.rows) {
+            const long long orow = q.verify ? q.qbase + row / G : q.qbase;
+            const int hq = h * G + (q.verify ? row % G : row);
+            const float inv = 1.f / ltot[mt][hh];
+            uint16_t* dst = p.out + (size_t(orow) * p.hq + hq) * kHeadDim + warp * 32 + tq * 2;
+#pragma unroll
+            for (int n = 0; n < 4; ++n)
+              *reinterpret_cast<uint32_t*>(dst + n * 8) =
+                  pack_bf16x2(o[mt][n][hh * 2] * inv, o[mt][n][hh * 2 + 1] * inv);
+            if (warp == 0 && tq == 0)
+              p.lse[size_t(orow) * p.hq + hq] = (m_run[mt][hh] + log2f(ltot[mt][hh])) * kLn2;
+          }
+        }
+    } else {
+      const size_t ustride = size_t(p.rows_max) * (kHeadDim + 2);
+      float* part = p.partials + size_t(u) * ustride;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = mt * 16 + g8 + hh * 8;
+          if (mt < mt_used && row < q.rows) {
+#pragma unroll
+            for (int n = 0; n < 4; ++n)
+              *reinterpret_cast<float2*>(part + row * kHeadDim + warp * 32 + n * 8 + tq * 2) =
+                  make_float2(o[mt][n][hh * 2], o[mt][n][hh * 2 + 1]);
+            if (warp == 0 && tq == 0) {
+              part[size_t(p.rows_max) * kHeadDim + row] = m_run[mt][hh];
+              part[size_t(p.rows_max) * (kHeadDim + 1) + row] = ltot[mt][hh];
+            }
+          }
+        }
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&p.merge_cnt[size_t(r) * p.hkv + h], 1);
+        s_misc[1] = (prev == nch - 1);
+      }
+      __syncthreads();
+      if (s_misc[1]) {
+        __threadfence();
+        merge_partials<MT>(p, q, h, u - c, nch);
+        if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
+      }
+    }
+  }
+
+  // ---- leave the queue counters at zero for the next launch ----
+  if (tid == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.q_done, 1u);
+    if (prev == gridDim.x - 1) {
+      atomicExch(p.q_next, 0u);
+      atomicExch(p.q_done, 0u);
+    }
+  }
+}
+
+template <int MT>
+cudaError_t launch_mt(const AttnParams& p, cudaStream_t stream) {
+  const size_t smem = Smem<MT>::bytes(p.batch);
+  cudaError_t e = cudaFuncSetAttribute(attn_persistent<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(Smem<MT>::bytes(SSPEC_MAX_BATCH)));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_persistent<MT>, kAttnThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int grid = device_sm_count() * per_sm;
+  attn_persistent<MT><<<grid, kAttnThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
+  const int mt = (p.rows_max + 15) / 16;
+  switch (mt) {
+    case 1: return launch_mt<1>(p, stream);
+    case 2: return launch_mt<2>(p, stream);
+    case 3: return launch_mt<3>(p, stream);
+    case 4: return launch_mt<4>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sspec

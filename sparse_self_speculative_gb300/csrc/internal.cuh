@@ -1,0 +1,118 @@
+// Internal declarations shared by the translation units of libsspec.so.
+// Nothing here is part of the C ABI (include/sspec.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sspec.h"
+
+namespace sspec {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 16;
+
+// ---- attention work decomposition -------------------------------------------------
+// A work unit is (request, kv head, chunk of kChunk tokens of that request's token
+// list).  Verification lists positions 0..L-1; a draft step lists its pillars then
+// its tail.  Chunks are merged through their (o, m, l) partial states.
+constexpr int kChunk = 512;
+constexpr int kTile = 64;          // tokens per pipeline stage
+constexpr int kStages = 3;         // cp.async pipeline depth
+constexpr int kAttnWarps = 4;
+constexpr int kAttnThreads = kAttnWarps * 32;
+
+// ---- selection work decomposition ----------------------------------------------------
+constexpr int kSelBlock = 4096;    // tokens averaged per unit
+constexpr int kSelThreads = 256;
+
+// ---- workspace layout ------------------------------------------------------------------
+// [0, 256)        header: error word and the persistent-kernel queue counters
+// [256, ...)      per (request, kv head) arrival counters: attention, then selection
+// [region, end)   attention partial states, or the averaged scores of selection
+struct WsHeader {
+  int32_t err;
+  int32_t pad0[3];
+  uint32_t attn_next, attn_done;
+  uint32_t sel_next, sel_done;
+};
+constexpr size_t kWsHeaderBytes = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline size_t ws_counter_bytes(int batch, int hkv) {
+  return align_up(size_t(batch) * size_t(hkv) * sizeof(int32_t), 256);
+}
+inline size_t ws_region_offset(int batch, int hkv) {
+  return kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv);
+}
+// bytes of one unit's partial state: O [rows][128] fp32, then m [rows], l [rows]
+inline size_t unit_partial_bytes(int rows_max) {
+  return size_t(rows_max) * (kHeadDim + 2) * sizeof(float);
+}
+
+// ---- kernel parameter blocks --------------------------------------------------------
+enum RequestMode : int { kAllVerify = 0, kAllDraft = 1, kByBucket = 2 };
+
+struct AttnParams {
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  const int32_t* block_table;
+  int max_pages;
+  int num_pages;
+  int hq, hkv, group;
+  float sm_scale;     // natural units
+  float scale_log2;   // sm_scale * log2(e)
+  int batch;
+  int nq;             // verification query rows per request
+  int mode;
+  const int32_t* bucket;
+  int verify_bucket;
+  const uint16_t* q;
+  const int64_t* q_off;       // nullable: rows r*nq (verify) or r (draft)
+  const int32_t* seq_lens;
+  const int32_t* sel_lens;
+  const int32_t* idx;
+  const int64_t* idx_off;
+  const int32_t* nsel;
+  uint16_t* out;
+  float* lse;
+  float* logits;              // nullable
+  const int64_t* logit_off;
+  // workspace
+  int32_t* err;
+  uint32_t* q_next;
+  uint32_t* q_done;
+  int32_t* merge_cnt;
+  float* partials;
+  long long unit_capacity;
+  int rows_max;               // partial-state row stride
+};
+
+struct SelectParams {
+  int batch, nq, hq, hkv, group;
+  float s;
+  const float* logits;
+  const int64_t* logit_off;
+  const float* lse;
+  const int64_t* q_off;
+  const int32_t* seq_lens;
+  float* scores;              // avg_scores or workspace region
+  long long score_capacity;   // floats available when scores lives in the workspace (-1: caller's)
+  int32_t* idx;
+  const int64_t* idx_off;
+  int32_t* nsel;
+  int32_t* err;
+  uint32_t* q_next;
+  uint32_t* q_done;
+  int32_t* cnt;
+};
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace sspec

@@ -1,0 +1,340 @@
+"""GPU parity of every entry point against the CPU oracle, through the C ABI,
+at sizes the oracle finishes in seconds that still span several tiles, chunks
+and ragged tails.
+
+Tolerances (stated by the problem, derived in the design doc for the rest):
+  attention outputs   |gpu - oracle| <= 2e-2 + 1e-2 * |oracle|
+  LSE                 |gpu - oracle| <= 1e-3
+  dumped logits       |gpu - oracle| <= 1e-4 + 1e-5 * |oracle|   (-inf exactly where masked)
+  averaged scores S   |gpu - oracle| <= 1e-4 * |oracle| + 1e-9
+  pillar indices      bit-exact against the oracle's Top-K of the GPU's own S
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import harness as hz
+
+pytestmark = pytest.mark.gpu
+
+OUT_ATOL, OUT_RTOL, LSE_TOL = 2e-2, 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import sparse_self_speculative_gb300 as ss
+    ss.lib()
+    torch.cuda.set_device(0)
+
+
+def _verify_batch(wl, nq):
+    import sparse_self_speculative_gb300 as ss
+    B, hq, hkv = wl.batch, wl.num_q_heads, wl.num_kv_heads
+    G = hq // hkv
+    dkv = hz.DeviceKV(wl, fill="host")
+    q = np.stack([wl.q_rows(r, np.arange(nq)) for r in range(B)])
+    L = wl.seq_lens.astype(np.int64)
+    loff = np.zeros(B + 1, dtype=np.int64)
+    loff[1:] = np.cumsum(hkv * nq * G * L)
+    d = dict(q=hz.bf16_i16(q).cuda(), seq=torch.from_numpy(wl.seq_lens).cuda(),
+             out=torch.empty((B, nq, hq, 128), dtype=torch.int16, device="cuda"),
+             lse=torch.empty((B, nq, hq), dtype=torch.float32, device="cuda"),
+             logits=torch.empty(int(loff[-1]), dtype=torch.float32, device="cuda"),
+             loff=torch.from_numpy(loff).cuda())
+    shape = ss.make_shape(hq, hkv)
+    ws = hz.zero_workspace(ss.sspec_workspace_size(shape, B, nq, int(L.sum())))
+    return dkv, q, loff, d, shape, ws
+
+
+def _run_verify(dkv, d, shape, ws, B, nq):
+    import sparse_self_speculative_gb300 as ss
+    ss.sspec_verify_attn(shape, dkv.kv(), B, nq, d["q"], d["seq"], d["out"], d["lse"], d["logits"], d["loff"], ws)
+    torch.cuda.synchronize()
+    assert hz.device_error(ws) == 0
+
+
+@pytest.mark.parametrize("hq,hkv,lens", [
+    (16, 8, [8, 9, 15, 16, 17, 63, 64, 65]),
+    (16, 8, [511, 512, 513, 1024, 1100, 2048]),
+    (32, 8, [8, 77, 600, 1537]),
+    (40, 8, [9, 129, 1030]),
+    (8, 1, [8, 300, 700]),          # G = 8: 64 query rows per KV head
+    (4, 4, [8, 1000]),              # G = 1
+])
+def test_verify_parity(hq, hkv, lens):
+    nq = 8
+    wl = synth.make_workload("v", 100 + hq + len(lens), hq, hkv, lens, plant="kv_per_head", plant_frac=0.02)
+    dkv, q, loff, d, shape, ws = _verify_batch(wl, nq)
+    _run_verify(dkv, d, shape, ws, wl.batch, nq)
+    out = hz.to_bits(d["out"])
+    lse = d["lse"].cpu().numpy()
+    logits = d["logits"].cpu().numpy()
+    G = hq // hkv
+    for r in range(wl.batch):
+        L = int(wl.seq_lens[r])
+        kf, vf = (oracle.bf16_bits_to_f64(wl.kv_rows(w, r, np.arange(L))) for w in "kv")
+        o_ref, l_ref, lg_ref = oracle.verify_attention(oracle.bf16_bits_to_f64(q[r]), kf, vf, hz.SCALE)
+        hz.check_close_bf16(out[r], o_ref, OUT_ATOL, OUT_RTOL)
+        assert np.abs(lse[r] - l_ref).max() <= LSE_TOL
+        lg = logits[loff[r]:loff[r + 1]].reshape(hkv, nq * G, L)
+        masked = np.isneginf(lg_ref)
+        np.testing.assert_array_equal(np.isneginf(lg), masked)
+        assert np.all(np.abs(lg[~masked] - lg_ref[~masked]) <= 1e-4 + 1e-5 * np.abs(lg_ref[~masked]))
+
+
+def test_verify_page_permutation_and_causal_bit_identity():
+    nq, hq, hkv = 8, 16, 8
+    lens = [700, 129]
+    wl = synth.make_workload("perm", 7, hq, hkv, lens)
+    dkv, q, loff, d, shape, ws = _verify_batch(wl, nq)
+    _run_verify(dkv, d, shape, ws, wl.batch, nq)
+    base = hz.to_bits(d["out"]).copy()
+    base_lse = d["lse"].cpu().numpy().copy()
+    # 1) move every page elsewhere in the pool: identical bits out
+    perm = torch.randperm(wl.num_pages, generator=torch.Generator().manual_seed(3)).cuda()
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(wl.num_pages, device="cuda")
+    k2 = torch.empty_like(dkv.k)
+    v2 = torch.empty_like(dkv.v)
+    k2[perm] = dkv.k
+    v2[perm] = dkv.v
+    bt2 = perm[dkv.block_table.long()].int()
+    dkv2 = hz.DeviceKV.__new__(hz.DeviceKV)
+    dkv2.k, dkv2.v, dkv2.block_table, dkv2.wl = k2, v2, bt2, wl
+    _run_verify(dkv2, d, shape, ws, wl.batch, nq)
+    np.testing.assert_array_equal(hz.to_bits(d["out"]), base)
+    np.testing.assert_array_equal(d["lse"].cpu().numpy(), base_lse)
+    # 2) overwrite the last cached token (seen only by the last verify query): other queries unchanged
+    r, L = 0, lens[0]
+    page = int(wl.block_table[r, (L - 1) // 16])
+    dkv.k[page, :, (L - 1) % 16] = 1234
+    dkv.v[page, :, (L - 1) % 16] = -4321
+    _run_verify(dkv, d, shape, ws, wl.batch, nq)
+    now = hz.to_bits(d["out"])
+    np.testing.assert_array_equal(now[r, :nq - 1], base[r, :nq - 1])
+    assert not np.array_equal(now[r, nq - 1], base[r, nq - 1])
+    np.testing.assert_array_equal(now[1], base[1])
+
+
+@pytest.mark.parametrize("hq,hkv,lens,steps", [
+    (16, 8, [64, 200, 1000, 2100, 4000], [0, 3, 7, 1, 5]),
+    (32, 8, [600, 5000, 130], [2, 0, 6]),
+    (40, 8, [3000, 77], [4, 7]),
+])
+def test_sparse_draft_parity(hq, hkv, lens, steps):
+    import sparse_self_speculative_gb300 as ss
+    k, s = 8, 0.05
+    wl = synth.make_workload("d", 300 + hq, hq, hkv, lens, plant="kv_per_head", plant_frac=0.02)
+    B = wl.batch
+    dkv = hz.DeviceKV(wl, fill="host")
+    L = wl.seq_lens.astype(np.int64)
+    sel = (L - np.asarray(steps) - 1).astype(np.int32)
+    nsel = np.array([oracle.pillar_count(s, int(x)) for x in sel], dtype=np.int32)
+    idx_off = np.zeros(B + 1, dtype=np.int64)
+    idx_off[1:] = np.cumsum(nsel.astype(np.int64) * hkv + 3 * hkv)      # some slack per head
+    idx = np.zeros(int(idx_off[-1]), dtype=np.int32)
+    pillars = {}
+    for r in range(B):
+        ps = hz.synthetic_pillars(wl.seed, r, hkv, int(sel[r]), int(nsel[r]))
+        stride = (idx_off[r + 1] - idx_off[r]) // hkv
+        for h in range(hkv):
+            idx[idx_off[r] + h * stride: idx_off[r] + h * stride + nsel[r]] = ps[h]
+        pillars[r] = ps
+    q = np.stack([wl.q_rows(r, np.arange(1))[0] for r in range(B)])
+    shape = ss.make_shape(hq, hkv)
+    out = torch.empty((B, hq, 128), dtype=torch.int16, device="cuda")
+    lse = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+    ws = hz.zero_workspace(ss.sspec_workspace_size(shape, B, 1, int(L.sum())))
+    ss.sspec_sparse_draft_attn(shape, dkv.kv(), B, hz.bf16_i16(q).cuda(), torch.from_numpy(wl.seq_lens).cuda(),
+                               torch.from_numpy(sel).cuda(), torch.from_numpy(idx).cuda(),
+                               torch.from_numpy(idx_off).cuda(), torch.from_numpy(nsel).cuda(), out, lse, ws)
+    torch.cuda.synchronize()
+    assert hz.device_error(ws) == 0
+    ob, lb = hz.to_bits(out), lse.cpu().numpy()
+    for r in range(B):
+        kf, vf = (oracle.bf16_bits_to_f64(wl.kv_rows(w, r, np.arange(int(L[r])))) for w in "kv")
+        o_ref, l_ref = oracle.sparse_draft_attention(oracle.bf16_bits_to_f64(q[r]), kf, vf, pillars[r],
+                                                     int(sel[r]), hz.SCALE)
+        hz.check_close_bf16(ob[r], o_ref, OUT_ATOL, OUT_RTOL)
+        assert np.abs(lb[r] - l_ref).max() <= LSE_TOL
+
+
+def test_sparse_with_every_token_equals_full_verify_bitwise():
+    """s = 1: the pillar set is every position, so the draft step attends to the
+    same ordered token list as one-query verification and must give the same bits."""
+    import sparse_self_speculative_gb300 as ss
+    hq, hkv = 16, 8
+    lens = [1500, 513, 64]
+    wl = synth.make_workload("s1", 9, hq, hkv, lens)
+    B = wl.batch
+    dkv = hz.DeviceKV(wl, fill="host")
+    L = wl.seq_lens.astype(np.int64)
+    sel = (L - 1).astype(np.int32)
+    idx_off = np.zeros(B + 1, dtype=np.int64)
+    idx_off[1:] = np.cumsum(sel.astype(np.int64) * hkv)
+    idx = np.concatenate([np.tile(np.arange(sel[r], dtype=np.int32), hkv) for r in range(B)])
+    q = np.stack([wl.q_rows(r, np.arange(1)) for r in range(B)])           # [B, 1, Hq, d]
+    shape = ss.make_shape(hq, hkv)
+    ws = hz.zero_workspace(ss.sspec_workspace_size(shape, B, 1, int(L.sum())))
+    out_s = torch.empty((B, hq, 128), dtype=torch.int16, device="cuda")
+    lse_s = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+    ss.sspec_sparse_draft_attn(shape, dkv.kv(), B, hz.bf16_i16(q[:, 0]).cuda(), torch.from_numpy(wl.seq_lens).cuda(),
+                               torch.from_numpy(sel).cuda(), torch.from_numpy(idx).cuda(),
+                               torch.from_numpy(idx_off).cuda(), torch.from_numpy(sel.copy()).cuda(), out_s, lse_s, ws)
+    out_v = torch.empty((B, 1, hq, 128), dtype=torch.int16, device="cuda")
+    lse_v = torch.empty((B, 1, hq), dtype=torch.float32, device="cuda")
+    ss.sspec_verify_attn(shape, dkv.kv(), B, 1, hz.bf16_i16(q).cuda(), torch.from_numpy(wl.seq_lens).cuda(),
+                         out_v, lse_v, None, None, ws)
+    torch.cuda.synchronize()
+    assert hz.device_error(ws) == 0
+    np.testing.assert_array_equal(hz.to_bits(out_s), hz.to_bits(out_v)[:, 0])
+    np.testing.assert_array_equal(lse_s.cpu().numpy(), lse_v.cpu().numpy()[:, 0])
+
+
+def _select_check(st, r, S_dev):
+    """GPU averages vs oracle averages; GPU indices vs the oracle's Top-K of the GPU averages."""
+    wl = st.wl
+    hq, hkv = wl.num_q_heads, wl.num_kv_heads
+    G, k = hq // hkv, st.k
+    L = int(wl.seq_lens[r])
+    lg = st.d_logits[st.logit_off[r]:st.logit_off[r + 1]].cpu().numpy().reshape(hkv, k * G, L)
+    lse = st.d_lse[st.q_off[r]:st.q_off[r + 1]].cpu().numpy()
+    kf, vf = st.kv_f64(r, np.arange(L))
+    _, l_ref, lg_ref = oracle.verify_attention(st.q_f64(r), kf, vf, hz.SCALE)
+    S_ref = oracle.average_scores(lg_ref, l_ref, G)
+    soff = st.logit_off[r] // (k * G)
+    Sg = S_dev[soff: soff + hkv * L].cpu().numpy().reshape(hkv, L).astype(np.float64)
+    assert np.all(np.abs(Sg - S_ref) <= 1e-4 * np.abs(S_ref) + 1e-9)
+    K = oracle.pillar_count(st.s, L)
+    assert int(st.d_nsel[r].item()) == K
+    idx = st.d_idx.cpu().numpy()
+    stride = (st.idx_off[r + 1] - st.idx_off[r]) // hkv
+    overlap = []
+    for h in range(hkv):
+        got = idx[st.idx_off[r] + h * stride: st.idx_off[r] + h * stride + K]
+        np.testing.assert_array_equal(got, oracle.top_k_pillars(Sg[h], K))
+        overlap.append(len(np.intersect1d(got, oracle.top_k_pillars(S_ref[h], K))) / K)
+    return float(np.mean(overlap))
+
+
+@pytest.mark.parametrize("hq,hkv,lens", [
+    (16, 8, [2048, 900, 8, 20, 4100]),
+    (32, 8, [5000, 1234]),
+    (40, 8, [777, 64]),
+])
+def test_fused_step_and_select_parity(hq, hkv, lens):
+    import sparse_self_speculative_gb300 as ss
+    k, s = 8, 0.05
+    B = len(lens) * 9
+    rng = np.random.default_rng(hq)
+    all_lens = np.concatenate([lens, rng.integers(40, 3000, size=B - len(lens))]).astype(np.int32)
+    wl = synth.make_workload("f", 500 + hq, hq, hkv, all_lens, plant="kv_per_head", plant_frac=0.01)
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="synthetic")
+    st.fused()
+    S = torch.empty(max(1, int(st.logit_off[-1]) // (k * hq // hkv)), dtype=torch.float32, device="cuda")
+    st.select(avg_scores=S)
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0
+    out, lse = hz.to_bits(st.d_out), st.d_lse.cpu().numpy()
+    overlaps = []
+    for r in range(B):
+        L = int(wl.seq_lens[r])
+        kf, vf = st.kv_f64(r, np.arange(L))
+        rows = slice(st.q_off[r], st.q_off[r + 1])
+        if st.is_verify[r]:
+            o_ref, l_ref, _ = oracle.verify_attention(st.q_f64(r), kf, vf, hz.SCALE)
+            overlaps.append(_select_check(st, r, S))
+        else:
+            o_ref, l_ref = oracle.sparse_draft_attention(st.q_f64(r)[0], kf, vf, st.pillars[r],
+                                                         int(st.sel_lens[r]), hz.SCALE)
+            o_ref, l_ref = o_ref[None], l_ref[None]
+        hz.check_close_bf16(out[rows], o_ref, OUT_ATOL, OUT_RTOL)
+        assert np.abs(lse[rows] - l_ref).max() <= LSE_TOL
+    # the GPU's pillars and the oracle's own Top-K agree almost everywhere (soft check)
+    assert np.mean(overlaps) > 0.98
+
+
+def test_fused_equals_separate_launches_bitwise():
+    """The fused launch computes each unit exactly as the single-template launches do."""
+    import sparse_self_speculative_gb300 as ss
+    k, s, hq, hkv = 8, 0.05, 32, 8
+    rng = np.random.default_rng(1)
+    lens = rng.integers(100, 4000, size=18).astype(np.int32)
+    wl = synth.make_workload("fs", 77, hq, hkv, lens)
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), len(lens))
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, pillars="synthetic")
+    st.fused()
+    torch.cuda.synchronize()
+    fused_out = hz.to_bits(st.d_out).copy()
+    fused_logits = st.d_logits.cpu().numpy().copy()
+    # same requests through the standalone entry points
+    vr = np.flatnonzero(st.is_verify)
+    dr = np.flatnonzero(~st.is_verify)
+    for r in vr:
+        out = torch.empty((1, k, hq, 128), dtype=torch.int16, device="cuda")
+        lse = torch.empty((1, k, hq), dtype=torch.float32, device="cuda")
+        lg = torch.empty(int(st.logit_off[r + 1] - st.logit_off[r]), dtype=torch.float32, device="cuda")
+        kv = ss.make_kv(dkv.k, dkv.v, dkv.block_table[r:r + 1].contiguous())
+        ss.sspec_verify_attn(st.shape, kv, 1, k, st.d_q[st.q_off[r]:st.q_off[r + 1]].contiguous(), st.d_seq[r:r + 1],
+                             out, lse, lg, torch.tensor([0, lg.numel()], dtype=torch.int64, device="cuda"), st.ws)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(hz.to_bits(out)[0], fused_out[st.q_off[r]:st.q_off[r + 1]])
+        np.testing.assert_array_equal(lg.cpu().numpy(), fused_logits[st.logit_off[r]:st.logit_off[r + 1]])
+    d = torch.from_numpy(dr).cuda()
+    kv = ss.make_kv(dkv.k, dkv.v, dkv.block_table[d].contiguous())
+    idx_off = np.zeros(len(dr) + 1, dtype=np.int64)
+    blocks = []
+    for i, r in enumerate(dr):
+        blocks.append(st.d_idx[st.idx_off[r]:st.idx_off[r + 1]])
+        idx_off[i + 1] = idx_off[i] + (st.idx_off[r + 1] - st.idx_off[r])
+    out = torch.empty((len(dr), hq, 128), dtype=torch.int16, device="cuda")
+    lse = torch.empty((len(dr), hq), dtype=torch.float32, device="cuda")
+    ss.sspec_sparse_draft_attn(st.shape, kv, len(dr), st.d_q[torch.from_numpy(st.q_off[dr]).cuda()].contiguous(),
+                               st.d_seq[d].contiguous(), st.d_sel[d].contiguous(), torch.cat(blocks),
+                               torch.from_numpy(idx_off).cuda(), st.d_nsel[d].contiguous(), out, lse, st.ws)
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0
+    np.testing.assert_array_equal(hz.to_bits(out), fused_out[st.q_off[dr]])
+
+
+def test_select_ties_go_to_lower_positions():
+    """Constant keys make every query row uniform over its visible prefix, so S is a
+    step function with long runs of exactly equal values; the kept positions must be
+    the lowest of the tied run."""
+    import sparse_self_speculative_gb300 as ss
+    hq, hkv, k, s = 16, 8, 8, 0.05
+    L = 3000
+    wl = synth.make_workload("ties", 5, hq, hkv, [L])
+    dkv = hz.DeviceKV(wl, fill="host")
+    # make every K row of the request equal to its first row
+    pages = wl.block_table[0, : (L + 15) // 16]
+    first = dkv.k[int(pages[0]), :, 0, :].clone()
+    dkv.k[torch.from_numpy(pages).long().cuda()] = first[None, :, None, :]
+    st = hz.UnifiedStep(wl, dkv, k, s, [0], pillars="synthetic")
+    st.fused()
+    S = torch.empty(hkv * L, dtype=torch.float32, device="cuda")
+    st.select(avg_scores=S)
+    torch.cuda.synchronize()
+    K = oracle.pillar_count(s, L)
+    idx = st.d_idx.cpu().numpy()
+    Sg = S.cpu().numpy().reshape(hkv, L)
+    for h in range(hkv):
+        got = idx[h * K:(h + 1) * K]
+        np.testing.assert_array_equal(got, oracle.top_k_pillars(Sg[h], K))
+        np.testing.assert_array_equal(got, np.arange(K))     # all of [0, L-k] tie; lowest win
+
+
+def test_device_generator_matches_host():
+    wl = synth.make_workload("gen", 31, 16, 8, [37, 300, 16, 1], plant="kv_per_head", plant_frac=0.05)
+    a = hz.DeviceKV(wl, fill="device")
+    for which, t in (("k", a.k), ("v", a.v)):
+        host = wl.paged_cache(which)
+        np.testing.assert_array_equal(hz.to_bits(t), host)
