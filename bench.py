@@ -205,6 +205,7 @@ def run_ours(args, world, rank, local):
         st.fused()
         st.select()
 
+    clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -217,16 +218,16 @@ def run_ours(args, world, rank, local):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        start.record(stream)
-        for i in range(args.steps):
-            ev_f0[i].record(stream)
-            st.fused()
-            ev_f1[i].record(stream)
-            st.select()
-            ev_s1[i].record(stream)
-        stop.record(stream)
-        torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        ev_f0[i].record(stream)
+        st.fused()
+        ev_f1[i].record(stream)
+        st.select()
+        ev_s1[i].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk.__exit__()
     barrier(world)
     total_ms = start.elapsed_time(stop)
     fused_ms = [a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)]
@@ -417,7 +418,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)

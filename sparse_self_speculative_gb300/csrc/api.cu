@@ -131,6 +131,7 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
   p.partials = reinterpret_cast<float*>(w.region);
   p.rows_max = any_verify ? nq * G : G;
   if (p.rows_max < G) p.rows_max = G;
+  p.unit_stride = (long long)unit_partial_floats(p.rows_max);
   p.unit_capacity = (long long)(w.region_bytes / unit_partial_bytes(p.rows_max));
   return launch_attention(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSPEC_OK
                                                                                      : SSPEC_ERR_CUDA;

@@ -82,6 +82,7 @@ __device__ bool load_req(const AttnParams& p, int r, Req& q, bool report) {
     if (!bad && q.nsel > q.idx_stride) bad |= SSPEC_DEVERR_RANGE;
     q.T = q.nsel + (q.L - q.sel_len);
   }
+  if (!bad && q.T > kMaxChunks * kChunk) bad |= SSPEC_DEVERR_LENGTH;
   if (bad && report) atomicOr(p.err, bad);
   return bad == 0;
 }
@@ -113,32 +114,71 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch) {
   return uint32_t(row * (kTile * 2) + ((ch ^ (row & 7)) << 4));
 }
 
+// Merge the nch partial states of one (request, kv head).  `scratch` is free shared
+// memory (the K/V ring) large enough for nch * rows weights plus 2 * rows floats.
 template <int MT>
-__device__ void merge_partials(const AttnParams& p, const Req& q, int h, long long u0, int nch) {
-  const size_t ustride = size_t(p.rows_max) * (kHeadDim + 2);
+__device__ void merge_partials(const AttnParams& p, const Req& q, int h, long long u0, int nch,
+                               float* scratch) {
+  const size_t ustride = size_t(p.unit_stride);
   const float* base = p.partials + size_t(u0) * ustride;
-  const int G = p.group;
-  for (int e = threadIdx.x; e < q.rows * (kHeadDim / 2); e += kAttnThreads) {
-    const int row = e / (kHeadDim / 2);
-    const int d = (e % (kHeadDim / 2)) * 2;
+  const int G = p.group, rows = q.rows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* sw = scratch;                       // [nch][rows] weights
+  float* s_inv = scratch + nch * rows;       // [rows] 1 / sum
+  float* s_lse = s_inv + rows;               // [rows]
+  for (int e = tid; e < nch * rows; e += kAttnThreads) {
+    const int c = e / rows, row = e - c * rows;
+    sw[e] = __ldcg(base + c * ustride + size_t(p.rows_max) * kHeadDim + row);
+  }
+  __syncthreads();
+  for (int row = warp; row < rows; row += kAttnWarps) {
     float M = -INFINITY;
-    for (int c = 0; c < nch; ++c)
-      M = fmaxf(M, __ldcg(base + c * ustride + size_t(p.rows_max) * kHeadDim + row));
-    float lsum = 0.f, o0 = 0.f, o1 = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const float* pc = base + c * ustride;
-      const float w = exp2f(__ldcg(pc + size_t(p.rows_max) * kHeadDim + row) - M);
-      lsum += w * __ldcg(pc + size_t(p.rows_max) * (kHeadDim + 1) + row);
-      const float2 ov = __ldcg(reinterpret_cast<const float2*>(pc + row * kHeadDim + d));
-      o0 += w * ov.x;
-      o1 += w * ov.y;
+    for (int c = lane; c < nch; c += 32) M = fmaxf(M, sw[c * rows + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float ls = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+      const float w = exp2f(sw[c * rows + row] - M);
+      ls += w * __ldcg(base + c * ustride + size_t(p.rows_max) * (kHeadDim + 1) + row);
+      sw[c * rows + row] = w;
     }
-    const float inv = 1.f / lsum;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if (lane == 0) {
+      s_inv[row] = 1.f / ls;
+      s_lse[row] = (M + log2f(ls)) * kLn2;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < rows * (kHeadDim / 4); e += kAttnThreads) {
+    const int row = e / (kHeadDim / 4);
+    const int d = (e % (kHeadDim / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* src = base + row * kHeadDim + d;
+    int c = 0;
+    for (; c + 4 <= nch; c += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __ldcg(reinterpret_cast<const float4*>(src + (c + i) * ustride));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float w = sw[(c + i) * rows + row];
+        acc.x += w * v[i].x; acc.y += w * v[i].y; acc.z += w * v[i].z; acc.w += w * v[i].w;
+      }
+    }
+    for (; c < nch; ++c) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + c * ustride));
+      const float w = sw[c * rows + row];
+      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    }
+    const float inv = s_inv[row];
     const long long orow = q.verify ? q.qbase + row / G : q.qbase;
     const int hq = h * G + (q.verify ? row % G : row);
-    *reinterpret_cast<uint32_t*>(p.out + (size_t(orow) * p.hq + hq) * kHeadDim + d) =
-        pack_bf16x2(o0 * inv, o1 * inv);
-    if (d == 0) p.lse[size_t(orow) * p.hq + hq] = (M + log2f(lsum)) * kLn2;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(p.out + (size_t(orow) * p.hq + hq) * kHeadDim + d) = pk;
+    if (d == 0) p.lse[size_t(orow) * p.hq + hq] = s_lse[row];
   }
 }
 
@@ -479,7 +519,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
           }
         }
     } else {
-      const size_t ustride = size_t(p.rows_max) * (kHeadDim + 2);
+      const size_t ustride = size_t(p.unit_stride);
       float* part = p.partials + size_t(u) * ustride;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -506,7 +546,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
       __syncthreads();
       if (s_misc[1]) {
         __threadfence();
-        merge_partials<MT>(p, q, h, u - c, nch);
+        merge_partials<MT>(p, q, h, u - c, nch, reinterpret_cast<float*>(smem + S::off_k));
         if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
       }
     }

@@ -17,7 +17,8 @@ constexpr int kPage = 16;
 // A work unit is (request, kv head, chunk of kChunk tokens of that request's token
 // list).  Verification lists positions 0..L-1; a draft step lists its pillars then
 // its tail.  Chunks are merged through their (o, m, l) partial states.
-constexpr int kChunk = 512;
+constexpr int kChunk = 1024;
+constexpr int kMaxChunks = 256;    // per (request, kv head): bounds the merge scratch
 constexpr int kTile = 64;          // tokens per pipeline stage
 constexpr int kStages = 3;         // cp.async pipeline depth
 constexpr int kAttnWarps = 4;
@@ -25,7 +26,8 @@ constexpr int kAttnThreads = kAttnWarps * 32;
 
 // ---- selection work decomposition ----------------------------------------------------
 constexpr int kSelBlock = 4096;    // tokens averaged per unit
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 512;
+constexpr int kSelSmemScores = 40960;  // averages of one head held in shared memory for Top-K
 
 // ---- workspace layout ------------------------------------------------------------------
 // [0, 256)        header: error word and the persistent-kernel queue counters
@@ -47,10 +49,12 @@ inline size_t ws_counter_bytes(int batch, int hkv) {
 inline size_t ws_region_offset(int batch, int hkv) {
   return kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv);
 }
-// bytes of one unit's partial state: O [rows][128] fp32, then m [rows], l [rows]
-inline size_t unit_partial_bytes(int rows_max) {
-  return size_t(rows_max) * (kHeadDim + 2) * sizeof(float);
+// one unit's partial state: O [rows][128] fp32, then m [rows], l [rows]; the stride
+// is padded to 4 floats so every O row starts 16-byte aligned
+inline size_t unit_partial_floats(int rows_max) {
+  return (size_t(rows_max) * (kHeadDim + 2) + 3) / 4 * 4;
 }
+inline size_t unit_partial_bytes(int rows_max) { return unit_partial_floats(rows_max) * sizeof(float); }
 
 // ---- kernel parameter blocks --------------------------------------------------------
 enum RequestMode : int { kAllVerify = 0, kAllDraft = 1, kByBucket = 2 };
@@ -87,7 +91,8 @@ struct AttnParams {
   int32_t* merge_cnt;
   float* partials;
   long long unit_capacity;
-  int rows_max;               // partial-state row stride
+  int rows_max;               // rows of a partial state
+  long long unit_stride;      // floats between consecutive partial states
 };
 
 struct SelectParams {

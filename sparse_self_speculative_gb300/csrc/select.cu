@@ -58,11 +58,12 @@ __device__ bool load_sel_req(const SelectParams& p, int r, SelReq& q, bool repor
   return bad == 0;
 }
 
-// Top-K of S[0..L) (fp32, >= 0) into out[0..K), ascending by position.
-__device__ void topk_ascending(const float* S, int L, int K, int32_t* out, uint32_t* hist,
-                              int* s_misc, int* s_warp) {
+// Top-K of S[0..L) (fp32, >= 0) into out[0..K), ascending by position.  The keys are
+// read through `key(t)`, which returns the bit pattern of S[t] (shared or global memory).
+template <typename KeyFn>
+__device__ void topk_ascending(KeyFn key, int L, int K, int32_t* out, uint32_t* hist, int* s_misc,
+                              int* s_warp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
   uint32_t prefix = 0, mask = 0;
   int kr = K;
   for (int shift = 24; shift >= 0; shift -= 8) {
@@ -70,7 +71,7 @@ __device__ void topk_ascending(const float* S, int L, int K, int32_t* out, uint3
     __syncthreads();
     for (int base = 0; base < L; base += kSelThreads) {
       const int t = base + tid;
-      const uint32_t u = (t < L) ? __ldcg(U + t) : 0u;
+      const uint32_t u = (t < L) ? key(t) : 0u;
       const bool match = (t < L) && ((u & mask) == prefix);
       const unsigned act = __ballot_sync(0xffffffffu, match);
       if (match) {
@@ -80,15 +81,17 @@ __device__ void topk_ascending(const float* S, int L, int K, int32_t* out, uint3
       }
     }
     __syncthreads();
-    // thread tid owns digit 255 - tid; inclusive scan from the top digit down
+    // threads 0..255 own digit 255 - tid; exclusive scan from the top digit down
     const int dig = 255 - tid;
     int cnt = 0;
+    if (tid < 256) {
 #pragma unroll
-    for (int w = 0; w < kSelWarps; ++w) cnt += int(hist[w * 256 + dig]);
+      for (int w = 0; w < kSelWarps; ++w) cnt += int(hist[w * 256 + dig]);
+    }
     int total;
     const int excl = block_exclusive_scan<kSelThreads>(cnt, s_warp, &total);
     // excl = number of matching keys whose digit is above `dig`
-    if (excl < kr && kr <= excl + cnt) {
+    if (tid < 256 && excl < kr && kr <= excl + cnt) {
       s_misc[0] = dig;
       s_misc[1] = excl;
     }
@@ -105,7 +108,7 @@ __device__ void topk_ascending(const float* S, int L, int K, int32_t* out, uint3
   int run_sel = 0, run_eq = 0;
   for (int base = 0; base < L; base += kSelThreads) {
     const int t = base + tid;
-    const uint32_t u = (t < L) ? __ldcg(U + t) : 0u;
+    const uint32_t u = (t < L) ? key(t) : 0u;
     const bool gt = (t < L) && u > T;
     const bool eq = (t < L) && u == T;
     const unsigned beq = __ballot_sync(0xffffffffu, eq);
@@ -136,7 +139,9 @@ __device__ void topk_ascending(const float* S, int L, int K, int32_t* out, uint3
 }
 
 __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectParams p) {
-  extern __shared__ int32_t s_prefix[];
+  extern __shared__ __align__(16) uint32_t s_dyn[];
+  uint32_t* s_keys = s_dyn;                                              // kSelSmemScores
+  int32_t* s_prefix = reinterpret_cast<int32_t*>(s_dyn + kSelSmemScores); // batch + 1
   __shared__ uint32_t hist[kSelWarps * 256];
   __shared__ float s_lse[SSPEC_MAX_ROWS];
   __shared__ int s_warp[kSelWarps];
@@ -202,6 +207,7 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
     const int t1 = min(q.L, (b + 1) * kSelBlock);
     for (int t = b * kSelBlock + tid; t < t1; t += kSelThreads) {
       float acc = 0.f;
+#pragma unroll 8
       for (int row = 0; row < q.rows; ++row) acc += expf(__ldcs(lg + size_t(row) * q.L + t) - s_lse[row]);
       S[t] = acc * inv_rows;
     }
@@ -214,7 +220,28 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
     __syncthreads();
     if (s_misc[3]) {
       __threadfence();
-      topk_ascending(S, q.L, q.K, p.idx + q.ibase + h * q.istride, hist, s_misc, s_warp);
+      int32_t* out = p.idx + q.ibase + h * q.istride;
+      const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
+      if (q.L <= kSelSmemScores) {
+        // stage this head's averages in shared memory, many loads in flight per thread
+        for (int t0 = tid; t0 < q.L; t0 += kSelThreads * 4) {
+          uint32_t v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int t = t0 + i * kSelThreads;
+            v[i] = (t < q.L) ? __ldcg(U + t) : 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int t = t0 + i * kSelThreads;
+            if (t < q.L) s_keys[t] = v[i];
+          }
+        }
+        __syncthreads();
+        topk_ascending([&](int t) { return s_keys[t]; }, q.L, q.K, out, hist, s_misc, s_warp);
+      } else {
+        topk_ascending([&](int t) { return __ldcg(U + t); }, q.L, q.K, out, hist, s_misc, s_warp);
+      }
       if (tid == 0) {
         p.nsel[r] = q.K;
         p.cnt[size_t(r) * p.hkv + h] = 0;
@@ -235,13 +262,15 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
 }  // namespace
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
-  const size_t smem = size_t(p.batch + 1) * 4;
+  const size_t smem = size_t(kSelSmemScores) * 4 + size_t(p.batch + 1) * 4;
+  cudaError_t e = cudaFuncSetAttribute(select_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(size_t(kSelSmemScores) * 4 + size_t(SSPEC_MAX_BATCH + 1) * 4));
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_persistent, kSelThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_persistent, kSelThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int grid = device_sm_count() * (per_sm < 4 ? per_sm : 4);
+  const int grid = device_sm_count() * per_sm;
   select_persistent<<<grid, kSelThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
