@@ -67,7 +67,8 @@ enum {
   SSPEC_DEVERR_INDEX_OOB = 2,       /* pillar index outside [0, sel_len) */
   SSPEC_DEVERR_LENGTH = 4,          /* seq_len / sel_len / nsel inconsistent or too long */
   SSPEC_DEVERR_RANGE = 8,           /* logit / index range of a request too small */
-  SSPEC_DEVERR_WORKSPACE = 16       /* workspace too small for the lengths in device memory */
+  SSPEC_DEVERR_WORKSPACE = 16,      /* workspace too small for the lengths in device memory */
+  SSPEC_DEVERR_TIMEOUT = 32         /* an internal pipeline wait expired (the kernel stopped early) */
 };
 
 /* Largest batch one call accepts. */

@@ -27,6 +27,7 @@ SSPEC_DEVERR_INDEX_OOB = 2
 SSPEC_DEVERR_LENGTH = 4
 SSPEC_DEVERR_RANGE = 8
 SSPEC_DEVERR_WORKSPACE = 16
+SSPEC_DEVERR_TIMEOUT = 32
 SSPEC_MAX_BATCH = 1024
 SSPEC_MAX_ROWS = 64
 

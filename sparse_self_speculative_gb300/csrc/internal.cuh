@@ -116,6 +116,7 @@ struct SelectParams {
 
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 
 int device_sm_count();
