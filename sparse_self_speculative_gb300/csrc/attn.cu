@@ -185,7 +185,7 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
 template <int MT>
 __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams p) {
   using S = Smem<MT>;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sK = smem_addr(smem + S::off_k);
   const uint32_t sV = smem_addr(smem + S::off_v);
   const uint32_t sQ = smem_addr(smem + S::off_q);

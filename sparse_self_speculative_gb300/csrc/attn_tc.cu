@@ -13,10 +13,11 @@
 // token list), verification units first, popped from an atomic counter.  Each
 // CTA (one per SM) runs three roles that hand tiles of 128 tokens to each
 // other through mbarriers:
-//   producer warps (5-7): pops units, resolves page / row ids, stages
-//     the unit's query rows, and streams K and V tiles into a ring of 32 KiB
-//     stages in the order the MMA consumes them (K0, K1, V0, K2, V1, ...),
-//     continuing straight into the next unit;
+//   producer warps (5-9): pop units and, one unit ahead, resolve page / row
+//     ids and stage the unit's query rows; stream K and V tiles into a ring of
+//     32 KiB stages in the order the MMA consumes them (K0, K1, V0, K2, V1, ...),
+//     straight into the next unit: verification as 2D TMA page boxes issued from
+//     16 lanes, drafts as 16-byte cp.async gathers from all producer threads;
 //   MMA warp (warp 4, one thread): S^T = K Q^T into TMEM (M = 128 tokens,
 //     N = query rows padded to 16), then O^T += V^T P^T into TMEM (M = 128
 //     dims), both kind::f16 with bf16 operands in 128-byte-swizzled smem;
@@ -45,11 +46,12 @@ constexpr int kTileBytes = kT * 256;       // one K or V tile: 32 KiB
 constexpr int kHalfBytes = kT * 128;       // one 64-dim half of a tile
 constexpr int kUnit = 1024;                // entries per unit
 constexpr int kUnitTiles = kUnit / kT;
-constexpr int kThreadsTC = 256;
-constexpr int kProdThreads = 96;           // warps 5-7
+constexpr int kThreadsTC = 320;
+constexpr int kIssueWarp = 5;              // first producer warp
 constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;
 constexpr int kMaxN = 64;
+constexpr int kSlots = 3;                  // prepared-unit slots (producer runs a unit ahead)
+constexpr int kProdThreads = 160;          // warps 5-9
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
@@ -95,6 +97,15 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -102,6 +113,15 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// four rows (box height 1) gathered into four consecutive 128-byte smem rows
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, const int (&y)[4],
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3]), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -171,16 +191,16 @@ __host__ __device__ inline Plan make_plan(int nmax, int batch, int smem_limit) {
   Plan pl;
   pl.qbytes = nmax * 256;
   pl.pbytes = nmax * 256;
-  const int fixed = 2 * pl.qbytes + 2 * pl.pbytes + kUnit * 4 + 2 * (int)sizeof(UnitDesc) +
+  const int fixed = kSlots * pl.qbytes + 2 * pl.pbytes + kSlots * kUnit * 4 + kSlots * (int)sizeof(UnitDesc) +
                     2 * 4 * kMaxN * 4 + 512 + 64 * 8 + 2 * (batch + 1) * 4 + batch * 4 + 1024 + 1024;
   pl.stages = (smem_limit - fixed) / kTileBytes;
   if (pl.stages > 8) pl.stages = 8;
   pl.off_ring = 0;
   pl.off_q = pl.stages * kTileBytes;
-  pl.off_p = pl.off_q + 2 * pl.qbytes;
+  pl.off_p = pl.off_q + kSlots * pl.qbytes;
   pl.off_rows = pl.off_p + 2 * pl.pbytes;
-  pl.off_unit = pl.off_rows + kUnit * 4;
-  pl.off_red = pl.off_unit + 2 * (int)sizeof(UnitDesc);
+  pl.off_unit = pl.off_rows + kSlots * kUnit * 4;
+  pl.off_red = pl.off_unit + kSlots * (int)sizeof(UnitDesc);
   pl.off_misc = pl.off_red + 2 * 4 * kMaxN * 4;
   pl.off_bar = pl.off_misc + 512;
   pl.off_prefix = pl.off_bar + 64 * 8;
@@ -192,14 +212,14 @@ __host__ __device__ inline Plan make_plan(int nmax, int batch, int smem_limit) {
 enum : int {
   B_RING_FULL = 0,    // [8]
   B_RING_EMPTY = 8,   // [8]
-  B_UNIT_FULL = 16,   // [2]
-  B_UNIT_EMPTY = 18,  // [2]
-  B_S_FULL = 20,      // [2]
-  B_S_EMPTY = 22,     // [2]
-  B_P_FULL = 24,      // [2]
-  B_P_EMPTY = 26,     // [2]
-  B_O_FULL = 28,      // [2]
-  B_O_EMPTY = 30,     // [2]
+  B_UNIT_FULL = 16,   // [kSlots]
+  B_UNIT_EMPTY = 19,  // [kSlots]
+  B_S_FULL = 22,      // [2]
+  B_S_EMPTY = 24,     // [2]
+  B_P_FULL = 26,      // [2]
+  B_P_EMPTY = 28,     // [2]
+  B_O_FULL = 30,      // [2]
+  B_O_EMPTY = 32,     // [2]
 };
 
 struct TCMaps {
@@ -276,21 +296,22 @@ __device__ bool req_info(const AttnParams& p, int r, ReqInfo& q, bool report) {
   return bad == 0;
 }
 
-// ---- producer warpgroup ---------------------------------------------------------------
-__device__ void producer(const AttnParams& p, const TCMaps& maps, const Ctx& cx, long long total_v,
-                         long long total) {
-  const int pt = threadIdx.x - kProdWarp0 * 32;     // 0..95
+// ---- producer warps (5-7) ------------------------------------------------------------------
+// prepare_unit pops one unit and prepares it in slot un % kSlots: the page ids (verification)
+// or 256-byte row ids (draft) of its entries, their validity mask and the query rows of its
+// kv head in 128-byte-swizzled layout.  Returns 1 for a unit, 0 once the queue is empty (an
+// end marker is published), -1 after an abort.
+__device__ int prepare_unit(const AttnParams& p, const Ctx& cx, uint32_t un, long long total_v,
+                            long long total) {
+  const int pt = threadIdx.x - kIssueWarp * 32;     // 0..kProdThreads-1
   const Plan& pl = cx.pl;
-  int32_t* s_rows = reinterpret_cast<int32_t*>(cx.smem + pl.off_rows);
   const int32_t* s_pv = reinterpret_cast<const int32_t*>(cx.smem + pl.off_prefix);
   const int32_t* s_pd = s_pv + (p.batch + 1);
   volatile long long* s_pop = reinterpret_cast<volatile long long*>(cx.smem + pl.off_misc);   // [0], [1]
-  const uint32_t ring0 = smem_addr(cx.smem + pl.off_ring);
   const int G = p.group;
-  uint32_t job = 0;
-  for (uint32_t un = 0;; ++un) {
-    const int us = un & 1;
-    const uint32_t uph = (un >> 1) & 1;
+  {
+    const int us = un % kSlots;
+    const uint32_t uph = (un / kSlots) & 1;
     if (pt == 0) {
       wait_bar(cx, bar_addr(cx, B_UNIT_EMPTY + us), uph ^ 1);
       s_pop[0] = (long long)atomicAdd(p.q_next, 1u);
@@ -300,14 +321,15 @@ __device__ void producer(const AttnParams& p, const TCMaps& maps, const Ctx& cx,
     const long long u = s_pop[0];
     const bool aborted = s_pop[1] != 0;
     named_sync(2, kProdThreads);
-    if (aborted) return;
+    if (aborted) return -1;
     UnitDesc* D = reinterpret_cast<UnitDesc*>(cx.smem + pl.off_unit) + us;
+    int32_t* s_rows = reinterpret_cast<int32_t*>(cx.smem + pl.off_rows) + us * kUnit;
     if (u >= total) {
       if (pt == 0) {
         D->type = kEnd;
         mbar_arrive(bar_addr(cx, B_UNIT_FULL + us));
       }
-      return;
+      return 0;
     }
     // decode: verification units first, then drafts
     const int32_t* pre = u < total_v ? s_pv : s_pd;
@@ -327,7 +349,6 @@ __device__ void producer(const AttnParams& p, const TCMaps& maps, const Ctx& cx,
     const int ntok = max(1, min(q.T - tok0, kUnit));
     const int npad = (q.rows + 15) & ~15;
     const int ntiles = (ntok + kT - 1) / kT;
-    // page ids (verification) or row ids (draft) of this unit
     if (q.verify) {
       const int npg = (ntok + kPage - 1) / kPage;
       for (int i = pt; i < npg; i += kProdThreads) {
@@ -338,24 +359,32 @@ __device__ void producer(const AttnParams& p, const TCMaps& maps, const Ctx& cx,
         s_rows[i] = rid;
       }
     } else {
-      for (int base = 0; base < kUnit; base += kProdThreads) {
-        const int i = base + pt;
+      // all index loads first, then all block-table loads: many loads in flight per thread
+      constexpr int kPer = (kUnit + kProdThreads - 1) / kProdThreads;
+      int pos[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = k * kProdThreads + pt;
+        const int e = tok0 + i;
+        pos[k] = -1;
+        if (i < ntok) pos[k] = e < q.nsel ? __ldg(p.idx + q.idx_base + h * q.idx_stride + e) : q.sel_len + (e - q.nsel);
+      }
+      int pg[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = k * kProdThreads + pt;
+        const bool ok = i < ntok && pos[k] >= 0 && (tok0 + i >= q.nsel || pos[k] < q.sel_len);
+        if (i < ntok && !ok) atomicOr(p.err, SSPEC_DEVERR_INDEX_OOB);
+        pg[k] = ok ? __ldg(p.block_table + size_t(r) * p.max_pages + (pos[k] >> 4)) : -1;
+        if (!ok) pos[k] = -1;
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = k * kProdThreads + pt;
         int rid = -1;
-        if (i < ntok) {
-          const int e = tok0 + i;
-          int pos, bad = 0;
-          if (e < q.nsel) {
-            pos = p.idx[q.idx_base + h * q.idx_stride + e];
-            if (pos < 0 || pos >= q.sel_len) bad = SSPEC_DEVERR_INDEX_OOB;
-          } else {
-            pos = q.sel_len + (e - q.nsel);
-          }
-          if (!bad) {
-            const int pg = p.block_table[size_t(r) * p.max_pages + (pos >> 4)];
-            if (pg < 0 || pg >= p.num_pages) bad = SSPEC_DEVERR_PAGE_OOB;
-            else rid = (pg * p.hkv + h) * kPage + (pos & (kPage - 1));
-          }
-          if (bad) atomicOr(p.err, bad);
+        if (pos[k] >= 0) {
+          if (pg[k] < 0 || pg[k] >= p.num_pages) atomicOr(p.err, SSPEC_DEVERR_PAGE_OOB);
+          else rid = (pg[k] * p.hkv + h) * kPage + (pos[k] & (kPage - 1));
         }
         if (i < kUnit) s_rows[i] = rid;
         const unsigned vb = __ballot_sync(0xffffffffu, rid >= 0);
@@ -376,71 +405,102 @@ __device__ void producer(const AttnParams& p, const TCMaps& maps, const Ctx& cx,
       *reinterpret_cast<uint4*>(qs + half * (npad * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
     }
     fence_async_smem();
-    named_sync(2, kProdThreads);
     if (pt == 0) {
       D->type = q.verify ? kVerify : kDraft;
       D->r = r; D->h = h; D->c = c; D->nch = nch;
       D->rows = q.rows; D->npad = npad; D->ntok = ntok; D->tok0 = tok0; D->L = q.L;
       D->vis_base = q.L - p.nq; D->ntiles = ntiles;
       D->u = u; D->qbase = q.qbase; D->loff = q.loff;
-      mbar_arrive(bar_addr(cx, B_UNIT_FULL + us));
     }
-    // stream tiles in MMA order: K0, then (K_i, V_{i-1}) for i >= 1, then V_last
-    for (int step = 0; step <= ntiles; ++step) {
-#pragma unroll 1
-      for (int kv = 0; kv < 2; ++kv) {
-        if (kv == 0 && step >= ntiles) continue;
-        if (kv == 1 && step == 0) continue;
-        const int i = kv == 0 ? step : step - 1;
-        const CUtensorMap* page_map = kv == 0 ? &maps.k_page : &maps.v_page;
-        const CUtensorMap* row_map = kv == 0 ? &maps.k_row : &maps.v_row;
-        const uint32_t s = job % pl.stages;
-        const uint32_t ph = (job / pl.stages) & 1;
-        ++job;
-        const uint32_t full = bar_addr(cx, B_RING_FULL + s);
-        const uint32_t dst = ring0 + s * kTileBytes;
-        const int e0 = i * kT;
-        const int nrow = min(kT, ntok - e0);
-        if (q.verify) {
-          if (pt == 0) {
-            wait_bar(cx, bar_addr(cx, B_RING_EMPTY + s), ph ^ 1);
-            uint32_t bytes = 0;
-            for (int pg = 0; pg * kPage < nrow; ++pg)
-              if (s_rows[(e0 >> 4) + pg] >= 0) bytes += uint32_t(min(kPage, nrow - pg * kPage)) * 256u;
-            mbar_arrive_tx(full, bytes);
-            for (int pg = 0; pg * kPage < nrow; ++pg) {
-              const int rid = s_rows[(e0 >> 4) + pg];
-              const int nv = min(kPage, nrow - pg * kPage);
-              if (rid < 0) continue;
-              if (nv == kPage) {
-                tma_2d(dst + pg * kPage * 128, page_map, 0, rid, full);
-                tma_2d(dst + kHalfBytes + pg * kPage * 128, page_map, 64, rid, full);
-              } else {
-                for (int rr = 0; rr < nv; ++rr) {
-                  tma_2d(dst + (pg * kPage + rr) * 128, row_map, 0, rid + rr, full);
-                  tma_2d(dst + kHalfBytes + (pg * kPage + rr) * 128, row_map, 64, rid + rr, full);
-                }
-              }
-            }
-          }
+    // every producer thread reads the descriptor after this barrier
+    named_sync(2, kProdThreads);
+    if (pt == 0) mbar_arrive(bar_addr(cx, B_UNIT_FULL + us));
+  }
+  return 1;
+}
+
+__device__ __forceinline__ void issue_tile(const AttnParams& p, const TCMaps& maps, const Ctx& cx, const UnitDesc* D,
+                                           const int32_t* s_rows, int i, int kv, uint32_t job) {
+  const int pt = threadIdx.x - kIssueWarp * 32;
+  const int lane = pt & 31;
+  const Plan& pl = cx.pl;
+  const uint32_t s = job % pl.stages;
+  const uint32_t ph = (job / pl.stages) & 1;
+  const uint32_t full = bar_addr(cx, B_RING_FULL + s);
+  const uint32_t dst = smem_addr(cx.smem + pl.off_ring) + s * kTileBytes;
+  const int e0 = i * kT;
+  const int nrow = min(kT, D->ntok - e0);
+  if (D->type == kVerify) {
+    // whole page blocks: lanes 0-15 of warp 5 issue one (page, 64-dim half) box each
+    if (pt >= 32) return;
+    const CUtensorMap* page_map = kv == 0 ? &maps.k_page : &maps.v_page;
+    const CUtensorMap* row_map = kv == 0 ? &maps.k_row : &maps.v_row;
+    if (lane == 0) {
+      wait_bar(cx, bar_addr(cx, B_RING_EMPTY + s), ph ^ 1);
+      uint32_t bytes = 0;
+      for (int pg = 0; pg * kPage < nrow; ++pg)
+        if (s_rows[(e0 >> 4) + pg] >= 0) bytes += uint32_t(min(kPage, nrow - pg * kPage)) * 256u;
+      mbar_arrive_tx(full, bytes);
+    }
+    __syncwarp();
+    const int pg = lane >> 1, hf = lane & 1;
+    if (lane < 2 * (kT / kPage) && pg * kPage < nrow) {
+      const int rid = s_rows[(e0 >> 4) + pg];
+      const int nv = min(kPage, nrow - pg * kPage);
+      if (rid >= 0) {
+        if (nv == kPage) {
+          tma_2d(dst + hf * kHalfBytes + pg * kPage * 128, page_map, hf * 64, rid, full);
         } else {
-          if (pt == 0) {
-            wait_bar(cx, bar_addr(cx, B_RING_EMPTY + s), ph ^ 1);
-            int nvalid = 0;
-            for (int w = 0; w < kT / 32; ++w) nvalid += __popc(D->valid[(e0 >> 5) + w]);
-            mbar_arrive_tx(full, uint32_t(nvalid) * 256u);
-          }
-          named_sync(2, kProdThreads);
-          for (int rr = pt; rr < nrow; rr += kProdThreads) {
-            const int rid = s_rows[e0 + rr];
-            if (rid >= 0) {
-              tma_2d(dst + rr * 128, row_map, 0, rid, full);
-              tma_2d(dst + kHalfBytes + rr * 128, row_map, 64, rid, full);
-            }
-          }
+          for (int rr = 0; rr < nv; ++rr)
+            tma_2d(dst + hf * kHalfBytes + (pg * kPage + rr) * 128, row_map, hf * 64, rid + rr, full);
         }
       }
     }
+    __syncwarp();
+  } else {
+    // gathered 256-byte rows: all producer threads, 16-byte cp.async into the same
+    // 128-byte-swizzled layout; completion reaches the stage barrier via
+    // cp.async.mbarrier.arrive (slots of invalid rows keep earlier finite data)
+    if (pt == 0) wait_bar(cx, bar_addr(cx, B_RING_EMPTY + s), ph ^ 1);
+    named_sync(2, kProdThreads);
+    const uint16_t* cache = kv == 0 ? p.k_cache : p.v_cache;
+    for (int idx = pt; idx < nrow * 16; idx += kProdThreads) {
+      const int rr = idx >> 4, ch = idx & 15;
+      const int rid = s_rows[e0 + rr];
+      if (rid >= 0)
+        cp_async16(dst + (ch >> 3) * kHalfBytes + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4),
+                   cache + size_t(rid) * kHeadDim + ch * 8, true);
+    }
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(full) : "memory");
+    named_sync(2, kProdThreads);
+    if (pt == 0) mbar_arrive(full);
+  }
+}
+
+// Streams K and V tiles of the prepared units into the ring in the order the MMA consumes
+// them (K0, then K_i and V_{i-1}, then the last V), straight across unit boundaries, and
+// prepares the next unit after the first two tiles of the current one are in flight.
+__device__ void producer(const AttnParams& p, const TCMaps& maps, const Ctx& cx, long long total_v,
+                         long long total) {
+  uint32_t job = 0;
+  int have = prepare_unit(p, cx, 0, total_v, total);
+  for (uint32_t un = 0; have == 1; ++un) {
+    const UnitDesc* D = reinterpret_cast<const UnitDesc*>(cx.smem + cx.pl.off_unit) + (un % kSlots);
+    const int32_t* s_rows = reinterpret_cast<const int32_t*>(cx.smem + cx.pl.off_rows) + (un % kSlots) * kUnit;
+    const int ntiles = min(max(D->ntiles, 1), kUnitTiles);
+    int next = -2, jobs = 0;
+    for (int step = 0; step <= ntiles; ++step) {
+      for (int kv = 0; kv < 2; ++kv) {
+        if (kv == 0 && step >= ntiles) continue;
+        if (kv == 1 && step == 0) continue;
+        if (jobs == 2 && next == -2) next = prepare_unit(p, cx, un + 1, total_v, total);
+        issue_tile(p, maps, cx, D, s_rows, kv == 0 ? step : step - 1, kv, job);
+        ++job;
+        ++jobs;
+      }
+    }
+    if (next == -2) next = prepare_unit(p, cx, un + 1, total_v, total);
+    have = next;
   }
 }
 
@@ -452,18 +512,20 @@ __device__ void mma_issuer(const Ctx& cx, uint32_t tmem, int nv) {
   const uint32_t p0 = smem_addr(cx.smem + pl.off_p);
   uint32_t job = 0, g = 0;
   for (uint32_t un = 0;; ++un) {
-    const int us = un & 1;
-    const uint32_t uph = (un >> 1) & 1;
+    const int us = un % kSlots;
+    const uint32_t uph = (un / kSlots) & 1;
     wait_bar(cx, bar_addr(cx, B_UNIT_FULL + us), uph);
     if (*cx.abort) return;
     const UnitDesc* D = reinterpret_cast<const UnitDesc*>(cx.smem + pl.off_unit) + us;
+    const int ob = un & 1;
+    const uint32_t oph = (un >> 1) & 1;
     if (D->type == kEnd) return;
     const int N = min(max(D->npad, 16), nv);
     const int ntiles = min(max(D->ntiles, 1), kUnitTiles);
     const uint32_t id_qk = instr_desc(N, 0), id_pv = instr_desc(N, 1);
     const uint32_t qb = q0 + us * pl.qbytes;
-    const uint32_t o_col = tmem + 2 * kMaxN + us * kMaxN;
-    wait_bar(cx, bar_addr(cx, B_O_EMPTY + us), uph ^ 1);
+    const uint32_t o_col = tmem + 2 * kMaxN + ob * kMaxN;
+    wait_bar(cx, bar_addr(cx, B_O_EMPTY + ob), oph ^ 1);
     tc_fence_after();
     for (int i = 0; i <= ntiles; ++i) {
       if (i < ntiles) {
@@ -472,6 +534,7 @@ __device__ void mma_issuer(const Ctx& cx, uint32_t tmem, int nv) {
         const uint32_t gi = g + i, sb = gi & 1;
         wait_bar(cx, bar_addr(cx, B_RING_FULL + s), ph);
         wait_bar(cx, bar_addr(cx, B_S_EMPTY + sb), ((gi >> 1) & 1) ^ 1);
+        fence_async_smem();   // gathered rows were written by cp.async (generic proxy)
         tc_fence_after();
         const uint32_t kb = ring0 + s * kTileBytes;
 #pragma unroll
@@ -489,6 +552,7 @@ __device__ void mma_issuer(const Ctx& cx, uint32_t tmem, int nv) {
         const uint32_t gi = g + i - 1, pb = gi & 1;
         wait_bar(cx, bar_addr(cx, B_RING_FULL + s), ph);
         wait_bar(cx, bar_addr(cx, B_P_FULL + pb), (gi >> 1) & 1);
+        fence_async_smem();
         tc_fence_after();
         const uint32_t vb = ring0 + s * kTileBytes;
         const uint32_t pbuf = p0 + pb * pl.pbytes;
@@ -502,7 +566,7 @@ __device__ void mma_issuer(const Ctx& cx, uint32_t tmem, int nv) {
         mma_commit(bar_addr(cx, B_RING_EMPTY + s));
       }
     }
-    mma_commit(bar_addr(cx, B_O_FULL + us));
+    mma_commit(bar_addr(cx, B_O_FULL + ob));
     mma_commit(bar_addr(cx, B_UNIT_EMPTY + us));
     g += ntiles;
   }
@@ -580,9 +644,11 @@ __device__ void softmax_wg(const AttnParams& p, const Ctx& cx, uint32_t tmem) {
   const int G = p.group;
   uint32_t g = 0;
   for (uint32_t un = 0;; ++un) {
-    const int us = un & 1;
-    const uint32_t uph = (un >> 1) & 1;
+    const int us = un % kSlots;
+    const uint32_t uph = (un / kSlots) & 1;
     const UnitDesc* Dp = reinterpret_cast<const UnitDesc*>(cx.smem + pl.off_unit) + us;
+    const int ob = un & 1;
+    const uint32_t oph = (un >> 1) & 1;
     if (t == 0) {
       wait_bar(cx, bar_addr(cx, B_UNIT_FULL + us), uph);
       s_flag[0] = (*cx.abort || Dp->type == kEnd) ? 1 : 0;
@@ -624,46 +690,54 @@ __device__ void softmax_wg(const AttnParams& p, const Ctx& cx, uint32_t tmem) {
       const int e = i * kT + t;
       const bool valid = e < ntok && (verify || ((Dp->valid[e >> 5] >> (e & 31)) & 1u));
       const int pos = tok0 + e;
+      // verification: query row n (query j = n / G) sees pos iff j >= pos - vis_base
+      const int nmin = verify ? max(0, (pos - vis_base) * G) : 0;
+      if (dump && e < ntok) {
+        float* lp = p.logits + loff + size_t(h) * rows * L + pos;
 #pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        bool vis = valid && n < N;
-        if (verify) vis = vis && pos <= vis_base + n / G;
-        if (dump && n < rows && e < ntok)
-          p.logits[loff + (size_t(h) * rows + n) * L + pos] = vis ? s[n] * p.sm_scale : -INFINITY;
-        s[n] = vis ? s[n] * p.scale_log2 : -INFINITY;
-      }
-      // tile maximum per query row
-#pragma unroll
-      for (int n = 0; n < NV; ++n) {
-        if (n < N) {
-          const float v = warp_max(s[n]);
-          if (lane == 0) s_red[warp * kMaxN + n] = v;
+        for (int n = 0; n < NV; ++n) {
+          if (n < rows) *lp = (valid && n >= nmin) ? s[n] * p.sm_scale : -INFINITY;
+          lp += L;
         }
       }
-      named_sync(1, 128);
-      bool rescale = false;
+      bool over = false;
 #pragma unroll
       for (int n = 0; n < NV; ++n) {
-        float alpha = 1.f;
-        if (n < N) {
-          const float tm = fmaxf(fmaxf(s_red[n], s_red[kMaxN + n]), fmaxf(s_red[2 * kMaxN + n], s_red[3 * kMaxN + n]));
-          if (tm > m[n] + 8.f) {
-            alpha = exp2f(m[n] - tm);   // 0 while m = -inf
-            m[n] = tm;
-            l[n] *= alpha;
-            rescale = true;
+        s[n] = (valid && n < N && n >= nmin) ? s[n] * p.scale_log2 : -INFINITY;
+        over |= s[n] > m[n] + 8.f;
+      }
+      // the reference maximum only moves when some value exceeds it by more than 2^8
+      // (always on a unit's first tile); decided by one predicate-reducing barrier
+      const bool rescale = named_sync_or(1, 128, over);
+      if (rescale) {
+#pragma unroll
+        for (int n = 0; n < NV; ++n) {
+          if (n < N) {
+            const float v = warp_max(s[n]);
+            if (lane == 0) s_red[warp * kMaxN + n] = v;
           }
         }
-        if (t == n) s_alpha[n] = alpha;
-      }
-      named_sync(1, 128);   // s_red is rewritten next tile; s_alpha complete
-      if (rescale) {
+        named_sync(1, 128);
+#pragma unroll
+        for (int n = 0; n < NV; ++n) {
+          float alpha = 1.f;
+          if (n < N) {
+            const float tm = fmaxf(fmaxf(s_red[n], s_red[kMaxN + n]), fmaxf(s_red[2 * kMaxN + n], s_red[3 * kMaxN + n]));
+            if (tm > m[n] + 8.f) {
+              alpha = exp2f(m[n] - tm);   // 0 while m = -inf
+              m[n] = tm;
+              l[n] *= alpha;
+            }
+          }
+          if (t == n) s_alpha[n] = alpha;
+        }
+        named_sync(1, 128);   // s_red is rewritten next tile; s_alpha complete
         if (i > 0) {
           // the previous tile's P V must have landed before O is rescaled in place
           const uint32_t gp = gi - 1;
           wait_bar(cx, bar_addr(cx, B_P_EMPTY + (gp & 1)), (gp >> 1) & 1);
           tc_fence_after();
-          const uint32_t ocol = tmem + lane_off + 2 * kMaxN + us * kMaxN;
+          const uint32_t ocol = tmem + lane_off + 2 * kMaxN + ob * kMaxN;
 #pragma unroll
           for (int c16 = 0; c16 < NV / 16; ++c16) {
             if (c16 * 16 < N) {
@@ -711,14 +785,14 @@ __device__ void softmax_wg(const AttnParams& p, const Ctx& cx, uint32_t tmem) {
 #pragma unroll
     for (int n = 0; n < NV; ++n)
       l[n] = (n < N) ? s_red2[n] + s_red2[kMaxN + n] + s_red2[2 * kMaxN + n] + s_red2[3 * kMaxN + n] : 1.f;
-    wait_bar(cx, bar_addr(cx, B_O_FULL + us), uph);
+    wait_bar(cx, bar_addr(cx, B_O_FULL + ob), oph);
     tc_fence_after();
     float o[NV];
 #pragma unroll
     for (int c16 = 0; c16 < NV / 16; ++c16) {
       if (c16 * 16 < N) {
         float v[16];
-        tmem_ld16(tmem + lane_off + 2 * kMaxN + us * kMaxN + c16 * 16, v);
+        tmem_ld16(tmem + lane_off + 2 * kMaxN + ob * kMaxN + c16 * 16, v);
 #pragma unroll
         for (int k = 0; k < 16; ++k) o[c16 * 16 + k] = v[k];
       } else {
@@ -728,7 +802,7 @@ __device__ void softmax_wg(const AttnParams& p, const Ctx& cx, uint32_t tmem) {
     }
     tmem_wait_ld();
     tc_fence_before();
-    mbar_arrive(bar_addr(cx, B_O_EMPTY + us));
+    mbar_arrive(bar_addr(cx, B_O_EMPTY + ob));
     const int nch = Dp->nch, r = Dp->r, c = Dp->c;
     const long long qbase = Dp->qbase, uid = Dp->u;
     const int d = t;
@@ -802,9 +876,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc(const AttnParams p, con
       mbar_init(bar_addr(cx, B_RING_FULL + s), 1);
       mbar_init(bar_addr(cx, B_RING_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSlots; ++b) {
       mbar_init(bar_addr(cx, B_UNIT_FULL + b), 1);
       mbar_init(bar_addr(cx, B_UNIT_EMPTY + b), 2);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(bar_addr(cx, B_S_FULL + b), 1);
       mbar_init(bar_addr(cx, B_S_EMPTY + b), 128);
       mbar_init(bar_addr(cx, B_P_FULL + b), 128);
@@ -864,6 +940,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc(const AttnParams p, con
     total_v = 0;
   }
 
+  if (tid == kIssueWarp * 32) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.k_page) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.v_page) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.k_row) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.v_row) : "memory");
+  }
   if (warp < 4) {
     softmax_wg<NV>(p, cx, tmem);
   } else if (warp == kMmaWarp) {

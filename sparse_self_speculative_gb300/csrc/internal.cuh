@@ -20,7 +20,7 @@ constexpr int kPage = 16;
 constexpr int kChunk = 1024;
 constexpr int kMaxChunks = 256;    // per (request, kv head): bounds the merge scratch
 constexpr int kTile = 64;          // tokens per pipeline stage
-constexpr int kStages = 3;         // cp.async pipeline depth
+constexpr int kStages = 2;         // cp.async pipeline depth (two CTAs per SM for every shape)
 constexpr int kAttnWarps = 4;
 constexpr int kAttnThreads = kAttnWarps * 32;
 
