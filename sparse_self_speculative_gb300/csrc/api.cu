@@ -51,6 +51,7 @@ struct Ws {
   WsHeader* hdr;
   int32_t* attn_cnt;
   int32_t* sel_cnt;
+  uint32_t* sel_hist;
   uint8_t* region;
   size_t region_bytes;
 };
@@ -64,6 +65,7 @@ int carve(void* workspace, size_t ws_bytes, int batch, int hkv, Ws& w) {
   w.err = &w.hdr->err;
   w.attn_cnt = reinterpret_cast<int32_t*>(b + kWsHeaderBytes);
   w.sel_cnt = reinterpret_cast<int32_t*>(b + kWsHeaderBytes + ws_counter_bytes(batch, hkv));
+  w.sel_hist = reinterpret_cast<uint32_t*>(b + kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv));
   w.region = b + off;
   w.region_bytes = ws_bytes - off;
   return SSPEC_OK;
@@ -220,6 +222,7 @@ int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, fl
   p.q_next = &w.hdr->sel_next;
   p.q_done = &w.hdr->sel_done;
   p.cnt = w.sel_cnt;
+  p.hist = w.sel_hist;
   return launch_select(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSPEC_OK : SSPEC_ERR_CUDA;
 }
 

@@ -17,7 +17,7 @@ constexpr int kPage = 16;
 // A work unit is (request, kv head, chunk of kChunk tokens of that request's token
 // list).  Verification lists positions 0..L-1; a draft step lists its pillars then
 // its tail.  Chunks are merged through their (o, m, l) partial states.
-constexpr int kChunk = 1024;
+constexpr int kChunk = 768;
 constexpr int kMaxChunks = 256;    // per (request, kv head): bounds the merge scratch
 constexpr int kTile = 64;          // tokens per pipeline stage
 constexpr int kStages = 2;         // cp.async pipeline depth (two CTAs per SM for every shape)
@@ -27,11 +27,14 @@ constexpr int kAttnThreads = kAttnWarps * 32;
 // ---- selection work decomposition ----------------------------------------------------
 constexpr int kSelBlock = 4096;    // tokens averaged per unit
 constexpr int kSelThreads = 512;
-constexpr int kSelSmemScores = 40960;  // averages of one head held in shared memory for Top-K
+constexpr int kSelBits1 = 11;      // radix digits of the fp32 keys: bits 31..21, 20..10, 9..0
+constexpr int kSelBins = 1 << kSelBits1;
+constexpr int kSelSegment = 16384; // positions per compaction segment
 
 // ---- workspace layout ------------------------------------------------------------------
 // [0, 256)        header: error word and the persistent-kernel queue counters
 // [256, ...)      per (request, kv head) arrival counters: attention, then selection
+//                 per (request, kv head) histograms of the first radix digit (selection)
 // [region, end)   attention partial states, or the averaged scores of selection
 struct WsHeader {
   int32_t err;
@@ -46,8 +49,11 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t ws_counter_bytes(int batch, int hkv) {
   return align_up(size_t(batch) * size_t(hkv) * sizeof(int32_t), 256);
 }
+inline size_t ws_hist_bytes(int batch, int hkv) {
+  return size_t(batch) * size_t(hkv) * kSelBins * sizeof(uint32_t);
+}
 inline size_t ws_region_offset(int batch, int hkv) {
-  return kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv);
+  return kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv) + ws_hist_bytes(batch, hkv);
 }
 // one unit's partial state: O [rows][128] fp32, then m [rows], l [rows]; the stride
 // is padded to 4 floats so every O row starts 16-byte aligned
@@ -112,11 +118,11 @@ struct SelectParams {
   uint32_t* q_next;
   uint32_t* q_done;
   int32_t* cnt;
+  uint32_t* hist;             // [batch * hkv][kSelBins], zero between calls
 };
 
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
-cudaError_t launch_attention_tc(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 
 int device_sm_count();

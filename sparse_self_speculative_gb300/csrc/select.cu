@@ -5,13 +5,17 @@
 // Sec. 4.1).
 //
 // One persistent launch.  A unit averages kSelBlock positions of one
-// (request, kv head): a pure stream over the dumped logits.  The last unit of
-// a (request, head) to finish (atomic arrival counter, no waiting) runs the
-// Top-K of that head: an MSB-first radix select over the fp32 bit patterns of
-// the averages (all >= 0, so their unsigned order is their numeric order),
-// four 8-bit digits with warp-aggregated shared-memory histograms, then one
-// ordered compaction pass that keeps every position above the threshold and
-// the lowest positions equal to it, written ascending.
+// (request, kv head): a pure stream over the dumped logits, which also adds
+// the first radix digit (top 11 bits) of its averages to a per-head histogram
+// in the workspace.  The last unit of a (request, head) to finish (atomic
+// arrival counter, no waiting) runs the Top-K of that head: an MSB-first radix
+// select over the fp32 bit patterns of the averages (all >= 0, so their
+// unsigned order is their numeric order) that starts from the accumulated
+// histogram and needs two more passes over the averages (bits 20..10, 9..0),
+// then an ordered compaction: ballots turn each 32 positions into words of
+// "above the threshold" and "equal to it" bits, word-level scans give every
+// word its output offset and the rank of its tied positions, and the lowest
+// tied positions are kept so that equal scores go to the lower position.
 #include <cmath>
 
 #include "device_common.cuh"
@@ -58,95 +62,147 @@ __device__ bool load_sel_req(const SelectParams& p, int r, SelReq& q, bool repor
   return bad == 0;
 }
 
-// Top-K of S[0..L) (fp32, >= 0) into out[0..K), ascending by position.  The keys are
-// read through `key(t)`, which returns the bit pattern of S[t] (shared or global memory).
-template <typename KeyFn>
-__device__ void topk_ascending(KeyFn key, int L, int K, int32_t* out, uint32_t* hist, int* s_misc,
-                              int* s_warp) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int kr = K;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < kSelWarps * 256; i += kSelThreads) hist[i] = 0;
-    __syncthreads();
-    for (int base = 0; base < L; base += kSelThreads) {
-      const int t = base + tid;
-      const uint32_t u = (t < L) ? key(t) : 0u;
-      const bool match = (t < L) && ((u & mask) == prefix);
+
+// Counts, in s_hist, digit (u >> shift) & (nbins-1) of every key u of S[0..L) whose bits
+// under `mask` equal `prefix` (warp-aggregated shared-memory atomics).
+__device__ void digit_histogram(const uint32_t* U, int L, uint32_t mask, uint32_t prefix, int shift,
+                                uint32_t nbins, uint32_t* s_hist) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int base = 0; base < L; base += kSelThreads * 4) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = base + i * kSelThreads + tid;
+      u[i] = t < L ? __ldcg(U + t) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = base + i * kSelThreads + tid;
+      const bool match = t < L && (u[i] & mask) == prefix;
       const unsigned act = __ballot_sync(0xffffffffu, match);
       if (match) {
-        const uint32_t dig = (u >> shift) & 255u;
+        const uint32_t dig = (u[i] >> shift) & (nbins - 1);
         const unsigned peers = __match_any_sync(act, dig);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[warp * 256 + dig], uint32_t(__popc(peers)));
+        if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[dig], uint32_t(__popc(peers)));
+      }
+    }
+  }
+}
+
+// Finds the digit holding the kr-th largest key among those counted in s_hist[0..nbins):
+// returns it and the number of counted keys with a larger digit.
+__device__ void find_digit(const uint32_t* s_hist, uint32_t nbins, int kr, int* s_warp, int* s_out) {
+  const int tid = threadIdx.x;
+  const int per = int(nbins) / kSelThreads;           // bins per thread, from the top down
+  const int hi = int(nbins) - tid * per;              // this thread owns bins [hi - per, hi)
+  int c = 0;
+  for (int b = hi - 1; b >= hi - per; --b) c += int(s_hist[b]);
+  int total;
+  int run = block_exclusive_scan<kSelThreads>(c, s_warp, &total);
+  for (int b = hi - 1; b >= hi - per; --b) {
+    const int n = int(s_hist[b]);
+    if (run < kr && kr <= run + n) {
+      s_out[0] = b;
+      s_out[1] = run;
+    }
+    run += n;
+  }
+  __syncthreads();
+}
+
+// Top-K of S[0..L) (fp32, >= 0) into out[0..K), ascending by position.  `ghist` holds the
+// histogram of the top 11 bits of all L keys; it is read and cleared here.
+__device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, int32_t* out, uint32_t* s_hist,
+                              uint32_t* s_gt, uint32_t* s_eq, int* s_misc, int* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
+  // digit 1 (bits 31..21) from the accumulated histogram
+  for (int b = tid; b < kSelBins; b += kSelThreads) {
+    s_hist[b] = __ldcg(ghist + b);
+    ghist[b] = 0u;
+  }
+  __syncthreads();
+  int kr = K;
+  find_digit(s_hist, kSelBins, kr, s_warp, s_misc);
+  uint32_t prefix = uint32_t(s_misc[0]) << 21, mask = 0xFFE00000u;
+  kr -= s_misc[1];
+  __syncthreads();
+  // digits 2 (bits 20..10) and 3 (bits 9..0)
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+    const uint32_t nbins = pass == 0 ? 2048u : 1024u;
+    for (int b = tid; b < kSelBins; b += kSelThreads) s_hist[b] = 0u;
+    __syncthreads();
+    digit_histogram(U, L, mask, prefix, shift, nbins, s_hist);
+    __syncthreads();
+    find_digit(s_hist, nbins, kr, s_warp, s_misc);
+    prefix |= uint32_t(s_misc[0]) << shift;
+    mask |= (nbins - 1) << shift;
+    kr -= s_misc[1];
+    __syncthreads();
+  }
+  // prefix is now the K-th largest key T; keep every key above T and the kr
+  // lowest-position keys equal to T, written in position order
+  const uint32_t T = prefix;
+  int run_eq = 0, run_sel = 0;
+  for (int seg0 = 0; seg0 < L; seg0 += kSelSegment) {
+    const int nwords = min(kSelSegment, L - seg0 + 31) / 32;
+    for (int w0 = warp * 4; w0 < nwords; w0 += kSelWarps * 4) {
+      uint32_t u[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = seg0 + (w0 + i) * 32 + lane;
+        u[i] = (w0 + i < nwords && t < L) ? __ldcg(U + t) : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = seg0 + (w0 + i) * 32 + lane;
+        const unsigned g = __ballot_sync(0xffffffffu, t < L && u[i] > T);
+        const unsigned e = __ballot_sync(0xffffffffu, t < L && u[i] == T);
+        if (lane == 0 && w0 + i < nwords) {
+          s_gt[w0 + i] = g;
+          s_eq[w0 + i] = e;
+        }
       }
     }
     __syncthreads();
-    // threads 0..255 own digit 255 - tid; exclusive scan from the top digit down
-    const int dig = 255 - tid;
-    int cnt = 0;
-    if (tid < 256) {
-#pragma unroll
-      for (int w = 0; w < kSelWarps; ++w) cnt += int(hist[w * 256 + dig]);
+    // one word per thread: rank of its tied positions, then its output offset
+    const int w = tid;
+    const uint32_t gw = w < nwords ? s_gt[w] : 0u;
+    const uint32_t ew = w < nwords ? s_eq[w] : 0u;
+    int eq_tot;
+    const int eq_before = run_eq + block_exclusive_scan<kSelThreads>(__popc(ew), s_warp, &eq_tot);
+    int take = kr - eq_before;
+    take = take < 0 ? 0 : take;
+    uint32_t keep = 0u, rest = ew;
+    for (int i = 0; i < take && rest; ++i) {
+      const uint32_t low = rest & (0u - rest);
+      keep |= low;
+      rest ^= low;
     }
-    int total;
-    const int excl = block_exclusive_scan<kSelThreads>(cnt, s_warp, &total);
-    // excl = number of matching keys whose digit is above `dig`
-    if (tid < 256 && excl < kr && kr <= excl + cnt) {
-      s_misc[0] = dig;
-      s_misc[1] = excl;
+    uint32_t sw = gw | keep;
+    int sel_tot;
+    int pos = run_sel + block_exclusive_scan<kSelThreads>(__popc(sw), s_warp, &sel_tot);
+    while (sw) {
+      const int bit = __ffs(sw) - 1;
+      out[pos++] = seg0 + w * 32 + bit;
+      sw &= sw - 1u;
     }
-    __syncthreads();
-    const uint32_t d = uint32_t(s_misc[0]);
-    kr -= s_misc[1];
-    prefix |= d << shift;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  // prefix = the K-th largest key; take all keys above it and the kr lowest-position
-  // keys equal to it, in position order
-  const uint32_t T = prefix;
-  int run_sel = 0, run_eq = 0;
-  for (int base = 0; base < L; base += kSelThreads) {
-    const int t = base + tid;
-    const uint32_t u = (t < L) ? key(t) : 0u;
-    const bool gt = (t < L) && u > T;
-    const bool eq = (t < L) && u == T;
-    const unsigned beq = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) s_warp[warp] = __popc(beq);
-    __syncthreads();
-    int eq_before = run_eq + __popc(beq & lanemask_lt()), eq_tot = 0;
-#pragma unroll
-    for (int w = 0; w < kSelWarps; ++w) {
-      eq_before += (w < warp) ? s_warp[w] : 0;
-      eq_tot += s_warp[w];
-    }
-    const bool sel = gt || (eq && eq_before < kr);
-    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-    __syncthreads();
-    if (lane == 0) s_warp[warp] = __popc(bsel);
-    __syncthreads();
-    int pos = run_sel + __popc(bsel & lanemask_lt()), sel_tot = 0;
-#pragma unroll
-    for (int w = 0; w < kSelWarps; ++w) {
-      pos += (w < warp) ? s_warp[w] : 0;
-      sel_tot += s_warp[w];
-    }
-    if (sel) out[pos] = t;
-    run_sel += sel_tot;
     run_eq += eq_tot;
+    run_sel += sel_tot;
     __syncthreads();
   }
 }
 
 __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectParams p) {
-  extern __shared__ __align__(16) uint32_t s_dyn[];
-  uint32_t* s_keys = s_dyn;                                              // kSelSmemScores
-  int32_t* s_prefix = reinterpret_cast<int32_t*>(s_dyn + kSelSmemScores); // batch + 1
-  __shared__ uint32_t hist[kSelWarps * 256];
+  extern __shared__ int32_t s_prefix[];                   // batch + 1
+  __shared__ uint32_t s_hist[kSelBins];
+  __shared__ uint32_t s_gt[kSelSegment / 32], s_eq[kSelSegment / 32];
   __shared__ float s_lse[SSPEC_MAX_ROWS];
   __shared__ int s_warp[kSelWarps];
   __shared__ int s_misc[4];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int B = p.batch;
 
   {
@@ -194,8 +250,10 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
     const int local = u - s_prefix[r];
     const int h = local / nb, b = local % nb;
     const int G = p.group;
+    uint32_t* ghist = p.hist + (size_t(r) * p.hkv + h) * kSelBins;
 
-    // ---- average kSelBlock positions of head h ----
+    // ---- average kSelBlock positions of head h, histogram their top 11 bits ----
+    for (int i = tid; i < kSelBins; i += kSelThreads) s_hist[i] = 0u;
     if (tid < q.rows) {
       const int j = tid / G, g = tid % G;
       s_lse[tid] = p.lse[size_t(q.qbase + j) * p.hq + h * G + g];
@@ -205,11 +263,27 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
     float* S = p.scores + q.soff + size_t(h) * q.L;
     const float inv_rows = 1.f / float(q.rows);
     const int t1 = min(q.L, (b + 1) * kSelBlock);
-    for (int t = b * kSelBlock + tid; t < t1; t += kSelThreads) {
+    for (int base = b * kSelBlock; base < t1; base += kSelThreads) {
+      const int t = base + tid;
+      const bool valid = t < t1;
       float acc = 0.f;
+      if (valid) {
 #pragma unroll 8
-      for (int row = 0; row < q.rows; ++row) acc += expf(__ldcs(lg + size_t(row) * q.L + t) - s_lse[row]);
-      S[t] = acc * inv_rows;
+        for (int row = 0; row < q.rows; ++row) acc += expf(__ldcs(lg + size_t(row) * q.L + t) - s_lse[row]);
+        acc *= inv_rows;
+        S[t] = acc;
+      }
+      const unsigned act = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const uint32_t dig = __float_as_uint(acc) >> 21;
+        const unsigned peers = __match_any_sync(act, dig);
+        if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[dig], uint32_t(__popc(peers)));
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < kSelBins; i += kSelThreads) {
+      const uint32_t v = s_hist[i];
+      if (v) atomicAdd(ghist + i, v);
     }
     __syncthreads();
     if (tid == 0) {
@@ -220,28 +294,7 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
     __syncthreads();
     if (s_misc[3]) {
       __threadfence();
-      int32_t* out = p.idx + q.ibase + h * q.istride;
-      const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
-      if (q.L <= kSelSmemScores) {
-        // stage this head's averages in shared memory, many loads in flight per thread
-        for (int t0 = tid; t0 < q.L; t0 += kSelThreads * 4) {
-          uint32_t v[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int t = t0 + i * kSelThreads;
-            v[i] = (t < q.L) ? __ldcg(U + t) : 0u;
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int t = t0 + i * kSelThreads;
-            if (t < q.L) s_keys[t] = v[i];
-          }
-        }
-        __syncthreads();
-        topk_ascending([&](int t) { return s_keys[t]; }, q.L, q.K, out, hist, s_misc, s_warp);
-      } else {
-        topk_ascending([&](int t) { return __ldcg(U + t); }, q.L, q.K, out, hist, s_misc, s_warp);
-      }
+      topk_ascending(S, q.L, q.K, ghist, p.idx + q.ibase + h * q.istride, s_hist, s_gt, s_eq, s_misc, s_warp);
       if (tid == 0) {
         p.nsel[r] = q.K;
         p.cnt[size_t(r) * p.hkv + h] = 0;
@@ -262,12 +315,9 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
 }  // namespace
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
-  const size_t smem = size_t(kSelSmemScores) * 4 + size_t(p.batch + 1) * 4;
-  cudaError_t e = cudaFuncSetAttribute(select_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(size_t(kSelSmemScores) * 4 + size_t(SSPEC_MAX_BATCH + 1) * 4));
-  if (e != cudaSuccess) return e;
+  const size_t smem = size_t(p.batch + 1) * 4;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_persistent, kSelThreads, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_persistent, kSelThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int grid = device_sm_count() * per_sm;
