@@ -176,6 +176,34 @@ int sspec_sparse_draft_attn(const sspec_shape* shape, const sspec_paged_kv* kv, 
                             sspec_stream_t stream);
 
 /*
+ * Allocation-free sparse draft attention (the paper has no counterpart: this is
+ * a convenience of this library).  Same computation, inputs and outputs as
+ * sspec_sparse_draft_attn, for callers that cannot call cudaMalloc -- runtimes
+ * and plugin hosts that own all device memory through their own pool, or code
+ * that must not allocate -- and therefore cannot provide a workspace.
+ *   - Scratch is a fixed 32 MiB array in the library's device memory, held by
+ *     every GPU that loads the library until the process exits.  Requests whose
+ *     workspace (sspec_workspace_size(shape, batch, 1, total_tokens)) exceeds
+ *     it are rejected with SSPEC_ERR_WORKSPACE_TOO_SMALL before anything is
+ *     enqueued.  total_tokens bounds the sum over requests of
+ *     nsel + seq_len - sel_len.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call on a device shares the array, which keeps the previous call's
+ *     contents; each call clears the part that must start at zero with a
+ *     cudaMemsetAsync on `stream`.  Calls whose work overlaps on the GPU (other
+ *     streams, other host threads) race on the scratch: serialize them.
+ *   - dev_error: nullable device int32; receives this call's device error word
+ *     (SSPEC_DEVERR_* bits), copied on `stream` after the kernel.
+ * Nothing is allocated or freed and nothing synchronizes.
+ */
+int sspec_sparse_draft_attn_noalloc(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
+                                    const void* q, const int32_t* seq_lens, const int32_t* sel_lens,
+                                    const int32_t* idx, const int64_t* idx_off, const int32_t* nsel,
+                                    void* out, float* lse, int64_t total_tokens, int32_t* dev_error,
+                                    sspec_stream_t stream);
+
+/*
  * One unified-batch attention step in a single persistent launch
  * (Unified batch scheduler + fused attention kernel: draft sparse attention
  * and verify full attention of the same batch are dispatched to their own
