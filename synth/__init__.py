@@ -190,14 +190,15 @@ class Workload:
 
 
 def _plant_masks(rng: np.random.Generator, seq_lens: np.ndarray, hkv: int,
-                 plant: str, frac: float, count: int):
+                 plant: str, frac: float, count: int, limit: int = 0):
     total = int(seq_lens.sum())
     pk = np.zeros((total, hkv), dtype=np.uint8)
     pv = np.zeros((total, hkv), dtype=np.uint8)
     base = 0
     for L in seq_lens.tolist():
         if plant == "keys_all_heads" and count > 0 and L > 0:
-            pos = rng.choice(L, size=min(count, L), replace=False)
+            span = min(L, limit) if limit > 0 else L
+            pos = rng.choice(span, size=min(count, span), replace=False)
             pk[base + pos, :] = 1
         elif plant == "kv_per_head" and frac > 0 and L > 0:
             n = int(round(frac * L))
@@ -211,7 +212,7 @@ def _plant_masks(rng: np.random.Generator, seq_lens: np.ndarray, hkv: int,
 
 def make_workload(name: str, seed: int, num_q_heads: int, num_kv_heads: int,
                   seq_lens, plant: str = "none", plant_frac: float = 0.0,
-                  plant_count: int = 0, spare_pages: int = 0) -> Workload:
+                  plant_count: int = 0, spare_pages: int = 0, plant_limit: int = 0) -> Workload:
     """Lay out a batch in a paged pool with a seeded random page permutation."""
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     rng = np.random.default_rng(seed)
@@ -235,7 +236,7 @@ def make_workload(name: str, seed: int, num_q_heads: int, num_kv_heads: int,
     bt[bt < 0] = 0
     tok_base = np.zeros(B + 1, dtype=np.int64)
     tok_base[1:] = np.cumsum(seq_lens.astype(np.int64))
-    pk, pv = _plant_masks(rng, seq_lens, num_kv_heads, plant, plant_frac, plant_count)
+    pk, pv = _plant_masks(rng, seq_lens, num_kv_heads, plant, plant_frac, plant_count, plant_limit)
     return Workload(name, seed, num_q_heads, num_kv_heads, seq_lens, pk, pv, bt,
                     num_pages, page_req, page_idx, tok_base)
 
