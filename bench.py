@@ -439,6 +439,112 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+
+# --------------------------------------------------------------------------------------
+# sweep (Qwen3-8B attention shape): sparse draft vs full decode attention, and k-query
+# verification with the dump, over context x batch x sparsity x stride
+# --------------------------------------------------------------------------------------
+def run_sweep(args):
+    import torch
+
+    import oracle
+    import synth
+    import sparse_self_speculative_gb300 as ss
+    from tests import harness as hz
+
+    torch.cuda.set_device(0)
+    hq, hkv = 32, 8
+    G = hq // hkv
+    Ls = [int(x) for x in args.sweep_L.split(",")]
+    Bs = [int(x) for x in args.sweep_B.split(",")]
+    S_list = [0.01, 0.05, 0.1, 1.0]
+    K_list = [4, 8]
+    shape = ss.make_shape(hq, hkv)
+    row_bytes = hkv * 128 * 2 * 2
+
+    def timeit(f, n):
+        for _ in range(2):
+            f()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            f()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    for L in Ls:
+        for B in Bs:
+            kv_gb = B * L * row_bytes / 1e9
+            logit_gb = B * hkv * max(K_list) * G * L * 4 / 1e9
+            free = torch.cuda.mem_get_info()[0] / 1e9
+            if kv_gb + logit_gb + 0.05 * kv_gb + 2 > free:
+                print(json.dumps({"sweep": True, "L": L, "B": B, "skipped": f"needs {kv_gb + logit_gb:.0f} GB, "
+                                                                      f"{free:.0f} GB free"}), flush=True)
+                continue
+            wl = synth.make_workload("sweep", 5000 + L + B, hq, hkv, [L] * B)
+            dkv = hz.DeviceKV(wl, fill="device")
+            kv = dkv.kv()
+            d_seq = torch.from_numpy(wl.seq_lens).cuda()
+            n_it = max(3, min(20, int(2000 / max(1.0, kv_gb * 1000 / 5000))))
+            for k in K_list:
+                rng = np.random.default_rng(L * 7 + B + k)
+                # (iii) verification: k queries per request with the logit dump
+                q = torch.randn((B, k, hq, 128), device="cuda").to(torch.bfloat16).view(torch.int16)
+                out = torch.empty((B, k, hq, 128), dtype=torch.int16, device="cuda")
+                lse = torch.empty((B, k, hq), dtype=torch.float32, device="cuda")
+                loff = torch.arange(B + 1, dtype=torch.int64, device="cuda") * (hkv * k * G * L)
+                logits = torch.empty(B * hkv * k * G * L, dtype=torch.float32, device="cuda")
+                ws = hz.zero_workspace(ss.sspec_workspace_size(shape, B, k, B * L))
+                t_ver = timeit(lambda: ss.sspec_verify_attn(shape, kv, B, k, q, d_seq, out, lse, logits, loff, ws), n_it)
+                ver_bytes = B * L * row_bytes + B * hkv * k * G * L * 4
+                del logits
+                # (ii) full decode attention: one query over every token, no dump
+                q1 = q[:, :1].contiguous()
+                out1 = torch.empty((B, 1, hq, 128), dtype=torch.int16, device="cuda")
+                lse1 = torch.empty((B, 1, hq), dtype=torch.float32, device="cuda")
+                t_full = timeit(lambda: ss.sspec_verify_attn(shape, kv, B, 1, q1, d_seq, out1, lse1, None, None, ws), n_it)
+                full_bytes = B * L * row_bytes
+                assert hz.device_error(ws) == 0
+                # (i) sparse draft attention at each s, draft step j uniform over [0, k)
+                steps = rng.integers(0, k, size=B)
+                sel = (L - steps - 1).astype(np.int32)
+                qd = q[:, 0].contiguous()
+                outd = torch.empty((B, hq, 128), dtype=torch.int16, device="cuda")
+                lsed = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+                for s_ in S_list:
+                    nsel = np.array([oracle.pillar_count(s_, int(x)) for x in sel], dtype=np.int32)
+                    ioff = np.zeros(B + 1, dtype=np.int64)
+                    ioff[1:] = np.cumsum(nsel.astype(np.int64) * hkv)
+                    idx = np.empty(int(ioff[-1]), dtype=np.int32)
+                    for r in range(B):
+                        for h in range(hkv):
+                            a = ioff[r] + h * nsel[r]
+                            if s_ >= 1.0:
+                                idx[a:a + nsel[r]] = np.arange(nsel[r])
+                            else:
+                                idx[a:a + nsel[r]] = np.sort(rng.choice(int(sel[r]), int(nsel[r]), replace=False))
+                    d_idx = torch.from_numpy(idx).cuda()
+                    d_ioff = torch.from_numpy(ioff).cuda()
+                    d_nsel = torch.from_numpy(nsel).cuda()
+                    d_sel = torch.from_numpy(sel).cuda()
+                    wsd = hz.zero_workspace(ss.sspec_workspace_size(shape, B, 1, int(nsel.sum() + (L - sel).sum())))
+                    t_sp = timeit(lambda: ss.sspec_sparse_draft_attn(shape, kv, B, qd, d_seq, d_sel, d_idx, d_ioff,
+                                                                     d_nsel, outd, lsed, wsd), n_it)
+                    sp_bytes = int((nsel.astype(np.int64) + steps + 1).sum()) * row_bytes
+                    assert hz.device_error(wsd) == 0
+                    print(json.dumps({"sweep": True, "L": L, "B": B, "s": s_, "k": k,
+                                      "sparse_ms": t_sp, "sparse_gbs": sp_bytes / t_sp / 1e6,
+                                      "full_ms": t_full, "full_gbs": full_bytes / t_full / 1e6,
+                                      "speedup_sparse_vs_full": t_full / t_sp,
+                                      "verify_ms": t_ver, "verify_gbs": ver_bytes / t_ver / 1e6}), flush=True)
+                    del d_idx, wsd
+                del q, out, lse, ws
+            del dkv, kv
+            torch.cuda.empty_cache()
+    return 0
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,8 +555,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="first N requests of the workload (profiling cases)")
+    ap.add_argument("--sweep", action="store_true", help="context x batch x sparsity x stride sweep (JSON lines)")
+    ap.add_argument("--sweep-L", default="1024,4096,16384,65536,131072")
+    ap.add_argument("--sweep-B", default="1,16,64,256")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    if args.sweep:
+        return run_sweep(args)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         if rank == 0:

@@ -21,6 +21,7 @@
 // padded to 16.  The softmax is the usual running-max form; all warps share
 // the per-row maximum of each tile through shared memory.
 #include <cfloat>
+#include <climits>
 #include <cmath>
 
 #include "device_common.cuh"
@@ -328,7 +329,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
         for (int i = 0; i < 4; ++i) o[mt][n][i] = 0.f;
     }
     const bool dump = q.verify && p.logits != nullptr;
-    const int vis_base = q.L - p.nq;  // query j sees positions <= vis_base + j
+    // per query row of this thread: last visible position (verification: query j sees
+    // positions <= L - nq + j; a draft sees its whole list) and its logit row in the dump
+    int vis_lim[MT][2];
+    float* drow[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = mt * 16 + g8 + hh * 8;
+        vis_lim[mt][hh] = q.verify ? q.L - p.nq + row / G : INT_MAX;
+        drow[mt][hh] = (dump && row < q.rows) ? p.logits + q.loff + (size_t(h) * q.rows + row) * q.L : nullptr;
+      }
 
     for (int t = 0; t < ntiles; ++t) {
       cp_async_wait<kStages - 2>();
@@ -387,12 +399,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
           for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              const int row = mt * 16 + g8 + hh * 8;
               const float x = sacc[mt][nt][hh * 2 + ii];
-              bool vis = valid;
-              if (q.verify) vis = vis && pos <= vis_base + row / G;
-              if (dump && mt < mt_used && row < q.rows && i < ntok)
-                p.logits[q.loff + (size_t(h) * q.rows + row) * q.L + pos] = vis ? x * p.sm_scale : -INFINITY;
+              const bool vis = valid && pos <= vis_lim[mt][hh];
+              if (drow[mt][hh] != nullptr && i < ntok) drow[mt][hh][pos] = vis ? x * p.sm_scale : -INFINITY;
               const float s2 = vis ? x * p.scale_log2 : -INFINITY;
               sacc[mt][nt][hh * 2 + ii] = s2;
               rmax[mt][hh] = fmaxf(rmax[mt][hh], s2);
