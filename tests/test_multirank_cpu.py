@@ -22,7 +22,15 @@ dist.destroy_process_group()
 """
 
 
+def _free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
 def _torchrun(script_args, port, env_extra=None, timeout=240):
+    port = _free_port()
     env = dict(os.environ, ROOT=ROOT, CUDA_VISIBLE_DEVICES="")
     if env_extra:
         env.update(env_extra)
