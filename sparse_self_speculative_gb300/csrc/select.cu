@@ -25,6 +25,10 @@ namespace sspec {
 namespace {
 
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelPer = kSelBlock / kSelThreads;   // positions per thread in an averaging unit
+constexpr int kSelRowGroup = 2;                     // logit rows loaded together
+static_assert(kSelBlock % kSelThreads == 0, "a unit is a whole number of positions per thread");
+static_assert(SSPEC_MAX_ROWS % kSelRowGroup == 0 && SSPEC_MAX_ROWS <= kSelThreads, "row groups fit s_lse");
 
 struct SelReq {
   int L;
@@ -195,7 +199,7 @@ __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, in
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectParams p) {
+__global__ void __launch_bounds__(kSelThreads, 2) select_persistent(const SelectParams p) {
   extern __shared__ int32_t s_prefix[];                   // batch + 1
   __shared__ uint32_t s_hist[kSelBins];
   __shared__ uint32_t s_gt[kSelSegment / 32], s_eq[kSelSegment / 32];
@@ -254,28 +258,52 @@ __global__ void __launch_bounds__(kSelThreads) select_persistent(const SelectPar
 
     // ---- average kSelBlock positions of head h, histogram their top 11 bits ----
     for (int i = tid; i < kSelBins; i += kSelThreads) s_hist[i] = 0u;
-    if (tid < q.rows) {
+    if (tid < SSPEC_MAX_ROWS) {
+      // rows past q.rows (up to the next multiple of kSelRowGroup) get lse 0: their
+      // loads are masked to -inf, so they add exp(-inf) = 0
       const int j = tid / G, g = tid % G;
-      s_lse[tid] = p.lse[size_t(q.qbase + j) * p.hq + h * G + g];
+      s_lse[tid] = tid < q.rows ? p.lse[size_t(q.qbase + j) * p.hq + h * G + g] : 0.f;
     }
     __syncthreads();
     const float* lg = p.logits + q.loff + size_t(h) * q.rows * q.L;
     float* S = p.scores + q.soff + size_t(h) * q.L;
     const float inv_rows = 1.f / float(q.rows);
-    const int t1 = min(q.L, (b + 1) * kSelBlock);
-    for (int base = b * kSelBlock; base < t1; base += kSelThreads) {
-      const int t = base + tid;
-      const bool valid = t < t1;
-      float acc = 0.f;
-      if (valid) {
-#pragma unroll 8
-        for (int row = 0; row < q.rows; ++row) acc += expf(__ldcs(lg + size_t(row) * q.L + t) - s_lse[row]);
-        acc *= inv_rows;
-        S[t] = acc;
+    const int t_lo = b * kSelBlock;
+    const int t1 = min(q.L, t_lo + kSelBlock);
+    // Thread tid owns positions t_lo + tid + j * kSelThreads (coalesced across the warp).
+    // The rows are read kSelRowGroup at a time with every load of the group issued
+    // before the first is used, so each thread keeps kSelRowGroup * kSelPer loads in
+    // flight and a unit costs only rows / kSelRowGroup memory round trips.
+    const float* col = lg + t_lo + tid;      // this thread's first position in row 0
+    const int rem = t1 - t_lo - tid;          // position j * kSelThreads is valid iff below rem
+    float acc[kSelPer];
+#pragma unroll
+    for (int j = 0; j < kSelPer; ++j) acc[j] = 0.f;
+#pragma unroll 1
+    for (int r0 = 0; r0 < q.rows; r0 += kSelRowGroup) {
+      float v[kSelRowGroup][kSelPer];
+#pragma unroll
+      for (int i = 0; i < kSelRowGroup; ++i) {
+        const bool row_ok = r0 + i < q.rows;
+        const float* src = col + size_t(row_ok ? r0 + i : 0) * q.L;
+#pragma unroll
+        for (int j = 0; j < kSelPer; ++j) v[i][j] = (row_ok && j * kSelThreads < rem) ? __ldcs(src + j * kSelThreads) : -INFINITY;
       }
+#pragma unroll
+      for (int i = 0; i < kSelRowGroup; ++i) {
+        const float l = s_lse[r0 + i];
+#pragma unroll
+        for (int j = 0; j < kSelPer; ++j) acc[j] += expf(v[i][j] - l);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kSelPer; ++j) {
+      const bool valid = j * kSelThreads < rem;
+      const float a = acc[j] * inv_rows;
+      if (valid) S[t_lo + j * kSelThreads + tid] = a;
       const unsigned act = __ballot_sync(0xffffffffu, valid);
       if (valid) {
-        const uint32_t dig = __float_as_uint(acc) >> 21;
+        const uint32_t dig = __float_as_uint(a) >> 21;
         const unsigned peers = __match_any_sync(act, dig);
         if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[dig], uint32_t(__popc(peers)));
       }
