@@ -27,6 +27,7 @@ namespace {
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelPer = kSelBlock / kSelThreads;   // positions per thread in an averaging unit
 constexpr int kSelRowGroup = 2;                     // logit rows loaded together
+constexpr int kSelCand = 8192;                      // Top-K candidates held in shared memory
 static_assert(kSelBlock % kSelThreads == 0, "a unit is a whole number of positions per thread");
 static_assert(SSPEC_MAX_ROWS % kSelRowGroup == 0 && SSPEC_MAX_ROWS <= kSelThreads, "row groups fit s_lse");
 
@@ -114,10 +115,105 @@ __device__ void find_digit(const uint32_t* s_hist, uint32_t nbins, int kr, int* 
   __syncthreads();
 }
 
+// Top-K when the keys whose top digit is at least d1 (the digit of the K-th largest key)
+// number at most kSelCand: one pass over S collects their positions in position order,
+// the remaining two digits are found among their keys in shared memory, and the result
+// is filtered out of that ordered list.  kr is the rank of the K-th largest key among
+// the keys whose top digit is d1.
+__device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int kr, int ncand, int32_t* out,
+                                     uint32_t* s_hist, uint32_t* s_words, int* s_misc, int* s_warp, int32_t* s_pos,
+                                     uint32_t* s_key) {
+  constexpr int kWords = 8;   // ballot words a warp builds per round of loads
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // positions whose key has top digit >= d1, in position order
+  int run = 0;
+  for (int seg0 = 0; seg0 < L; seg0 += kSelSegment) {
+    const int nwords = (min(kSelSegment, L - seg0) + 31) / 32;
+    for (int w0 = warp * kWords; w0 < nwords; w0 += kSelWarps * kWords) {
+      uint32_t u[kWords];
+#pragma unroll
+      for (int i = 0; i < kWords; ++i) {
+        const int t = seg0 + (w0 + i) * 32 + lane;
+        u[i] = (w0 + i < nwords && t < L) ? __ldcg(U + t) : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < kWords; ++i) {
+        const int t = seg0 + (w0 + i) * 32 + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, w0 + i < nwords && t < L && (u[i] >> 21) >= d1);
+        if (lane == 0 && w0 + i < nwords) s_words[w0 + i] = m;
+      }
+    }
+    __syncthreads();
+    uint32_t wb = tid < nwords ? s_words[tid] : 0u;   // one word per thread
+    int tot;
+    int at = run + block_exclusive_scan<kSelThreads>(__popc(wb), s_warp, &tot);
+    while (wb) {
+      const int bit = __ffs(wb) - 1;
+      if (at < kSelCand) s_pos[at] = seg0 + tid * 32 + bit;
+      ++at;
+      wb &= wb - 1u;
+    }
+    run += tot;
+    __syncthreads();
+  }
+  // their keys (S is resident in L2)
+  for (int i0 = tid; i0 < ncand; i0 += kSelThreads * 4) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = i0 + i * kSelThreads < ncand ? __ldcg(U + s_pos[i0 + i * kSelThreads]) : 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i0 + i * kSelThreads < ncand) s_key[i0 + i * kSelThreads] = u[i];
+  }
+  __syncthreads();
+  // digits 2 (bits 20..10) and 3 (bits 9..0) of the K-th largest key
+  uint32_t prefix = d1 << 21, mask = 0xFFE00000u;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+    const uint32_t nbins = pass == 0 ? 2048u : 1024u;
+    for (int b = tid; b < kSelBins; b += kSelThreads) s_hist[b] = 0u;
+    __syncthreads();
+    for (int i = tid; i < ncand; i += kSelThreads) {
+      const uint32_t u = s_key[i];
+      if ((u & mask) == prefix) atomicAdd(&s_hist[(u >> shift) & (nbins - 1)], 1u);
+    }
+    __syncthreads();
+    find_digit(s_hist, nbins, kr, s_warp, s_misc);
+    prefix |= uint32_t(s_misc[0]) << shift;
+    mask |= (nbins - 1) << shift;
+    kr -= s_misc[1];
+    __syncthreads();
+  }
+  // keep every key above T and the kr lowest-position keys equal to T, in order:
+  // each thread filters a contiguous run of the ordered candidates
+  const uint32_t T = prefix;
+  const int per = (ncand + kSelThreads - 1) / kSelThreads;
+  const int i0 = min(ncand, tid * per), i1 = min(ncand, i0 + per);
+  int neq = 0;
+  for (int i = i0; i < i1; ++i) neq += s_key[i] == T;
+  int tot;
+  const int eq_before = block_exclusive_scan<kSelThreads>(neq, s_warp, &tot);
+  int nkeep = 0;
+  for (int i = i0, e = eq_before; i < i1; ++i) {
+    const uint32_t u = s_key[i];
+    nkeep += u > T || (u == T && e < kr);
+    e += u == T;
+  }
+  int at = block_exclusive_scan<kSelThreads>(nkeep, s_warp, &tot);
+  for (int i = i0, e = eq_before; i < i1; ++i) {
+    const uint32_t u = s_key[i];
+    if (u > T || (u == T && e < kr)) out[at++] = s_pos[i];
+    e += u == T;
+  }
+  __syncthreads();
+}
+
 // Top-K of S[0..L) (fp32, >= 0) into out[0..K), ascending by position.  `ghist` holds the
 // histogram of the top 11 bits of all L keys; it is read and cleared here.
 __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, int32_t* out, uint32_t* s_hist,
-                              uint32_t* s_gt, uint32_t* s_eq, int* s_misc, int* s_warp) {
+                              uint32_t* s_gt, uint32_t* s_eq, int* s_misc, int* s_warp, int32_t* s_pos,
+                              uint32_t* s_key) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
   // digit 1 (bits 31..21) from the accumulated histogram
@@ -130,7 +226,12 @@ __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, in
   find_digit(s_hist, kSelBins, kr, s_warp, s_misc);
   uint32_t prefix = uint32_t(s_misc[0]) << 21, mask = 0xFFE00000u;
   kr -= s_misc[1];
+  const int ncand = s_misc[1] + int(s_hist[s_misc[0]]);   // keys with top digit >= the K-th's
   __syncthreads();
+  if (ncand <= kSelCand) {
+    topk_from_candidates(U, L, prefix >> 21, kr, ncand, out, s_hist, s_gt, s_misc, s_warp, s_pos, s_key);
+    return;
+  }
   // digits 2 (bits 20..10) and 3 (bits 9..0)
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
@@ -200,7 +301,10 @@ __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, in
 }
 
 __global__ void __launch_bounds__(kSelThreads, 2) select_persistent(const SelectParams p) {
-  extern __shared__ int32_t s_prefix[];                   // batch + 1
+  extern __shared__ __align__(16) int32_t s_dyn[];
+  int32_t* s_pos = s_dyn;                                   // kSelCand candidate positions
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(s_dyn + kSelCand);   // and their keys
+  int32_t* s_prefix = s_dyn + 2 * kSelCand;                 // batch + 1 unit offsets
   __shared__ uint32_t s_hist[kSelBins];
   __shared__ uint32_t s_gt[kSelSegment / 32], s_eq[kSelSegment / 32];
   __shared__ float s_lse[SSPEC_MAX_ROWS];
@@ -322,7 +426,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_persistent(const Select
     __syncthreads();
     if (s_misc[3]) {
       __threadfence();
-      topk_ascending(S, q.L, q.K, ghist, p.idx + q.ibase + h * q.istride, s_hist, s_gt, s_eq, s_misc, s_warp);
+      topk_ascending(S, q.L, q.K, ghist, p.idx + q.ibase + h * q.istride, s_hist, s_gt, s_eq, s_misc, s_warp,
+                     s_pos, s_key);
       if (tid == 0) {
         p.nsel[r] = q.K;
         p.cnt[size_t(r) * p.hkv + h] = 0;
@@ -343,7 +448,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_persistent(const Select
 }  // namespace
 
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
-  const size_t smem = size_t(p.batch + 1) * 4;
+  const size_t smem = size_t(2 * kSelCand + p.batch + 1) * 4;
+  cudaError_t ea = cudaFuncSetAttribute(select_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (ea != cudaSuccess) return ea;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_persistent, kSelThreads, smem);
   if (e != cudaSuccess) return e;

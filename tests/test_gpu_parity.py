@@ -305,13 +305,14 @@ def test_fused_equals_separate_launches_bitwise():
     np.testing.assert_array_equal(hz.to_bits(out), fused_out[st.q_off[dr]])
 
 
-def test_select_ties_go_to_lower_positions():
+@pytest.mark.parametrize("L", [3000, 20000])
+def test_select_ties_go_to_lower_positions(L):
     """Constant keys make every query row uniform over its visible prefix, so S is a
     step function with long runs of exactly equal values; the kept positions must be
-    the lowest of the tied run."""
+    the lowest of the tied run.  At 20,000 tokens the tied run is longer than the
+    selection's shared-memory candidate list, so the multi-pass radix path runs."""
     import sparse_self_speculative_gb300 as ss
     hq, hkv, k, s = 16, 8, 8, 0.05
-    L = 3000
     wl = synth.make_workload("ties", 5, hq, hkv, [L])
     dkv = hz.DeviceKV(wl, fill="host")
     # make every K row of the request equal to its first row
@@ -330,6 +331,25 @@ def test_select_ties_go_to_lower_positions():
         got = idx[h * K:(h + 1) * K]
         np.testing.assert_array_equal(got, oracle.top_k_pillars(Sg[h], K))
         np.testing.assert_array_equal(got, np.arange(K))     # all of [0, L-k] tie; lowest win
+
+
+@pytest.mark.parametrize("L,s", [(12000, 0.05), (30000, 0.2), (30000, 0.4), (40960, 0.05)])
+def test_select_candidate_list_and_multipass_paths(L, s):
+    """Top-K through both selection paths: the keys at or above the K-th largest key's
+    top radix digit fit the shared-memory candidate list (short rows, small s), or do
+    not (s = 0.4 makes K = 12,000 alone exceed it)."""
+    import sparse_self_speculative_gb300 as ss
+    hq, hkv, k = 16, 8, 8
+    wl = synth.make_workload("cap", 900 + int(100 * s), hq, hkv, [L, 500], plant="kv_per_head", plant_frac=0.01)
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, [0, 3], pillars="synthetic")
+    st.fused()
+    S = torch.empty(max(1, int(st.logit_off[-1]) // (k * hq // hkv)), dtype=torch.float32, device="cuda")
+    st.select(avg_scores=S)
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0
+    assert st.is_verify[0]
+    assert _select_check(st, 0, S) > 0.98
 
 
 def test_device_generator_matches_host():
