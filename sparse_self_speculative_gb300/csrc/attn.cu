@@ -31,6 +31,7 @@ namespace sspec {
 namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazyMax = 8.f;   // log2 of the largest unnormalised probability
 constexpr int kRowBytes = kHeadDim * 2;  // one token row of one head: 256 B
 
 struct Req {
@@ -88,13 +89,14 @@ __device__ bool load_req(const AttnParams& p, int r, Req& q, bool report) {
   return bad == 0;
 }
 
-template <int MT>
+template <int MT, int W>
 struct Smem {
   static constexpr int kKV = kStages * kTile * kRowBytes;   // one of K or V ring
   static constexpr int kQ = MT * 16 * kRowBytes;
   static constexpr int kP = MT * 16 * kTile * 2;
   static constexpr int kRowIds = kChunk * 4;
-  static constexpr int kRed = kAttnWarps * MT * 16 * 4;
+  static constexpr int kRed = W * 16 * 4;                    // per-warp row maxima
+  static constexpr int kRedL = (kTile / 8) * MT * 16 * 4;    // row sums of each 8-token column group
   static constexpr int off_k = 0;
   static constexpr int off_v = off_k + kKV;
   static constexpr int off_q = off_v + kKV;
@@ -102,7 +104,7 @@ struct Smem {
   static constexpr int off_rows = off_p + kP;
   static constexpr int off_rmax = off_rows + kRowIds;
   static constexpr int off_rl = off_rmax + kRed;
-  static constexpr int off_prefix = off_rl + kRed;
+  static constexpr int off_prefix = off_rl + kRedL;
   static size_t bytes(int batch) { return off_prefix + size_t(batch + 1) * 4; }
 };
 
@@ -117,7 +119,7 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch) {
 
 // Merge the nch partial states of one (request, kv head).  `scratch` is free shared
 // memory (the K/V ring) large enough for nch * rows weights plus 2 * rows floats.
-template <int MT>
+template <int MT, int W>
 __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long long u0, int nch,
                                float* scratch) {
   const size_t ustride = size_t(p.unit_stride);
@@ -127,12 +129,12 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
   float* sw = scratch;                       // [nch][rows] weights
   float* s_inv = scratch + nch * rows;       // [rows] 1 / sum
   float* s_lse = s_inv + rows;               // [rows]
-  for (int e = tid; e < nch * rows; e += kAttnThreads) {
+  for (int e = tid; e < nch * rows; e += W * 32) {
     const int c = e / rows, row = e - c * rows;
     sw[e] = __ldcg(base + c * ustride + size_t(p.rows_max) * kHeadDim + row);
   }
   __syncthreads();
-  for (int row = warp; row < rows; row += kAttnWarps) {
+  for (int row = warp; row < rows; row += W) {
     float M = -INFINITY;
     for (int c = lane; c < nch; c += 32) M = fmaxf(M, sw[c * rows + row]);
 #pragma unroll
@@ -151,7 +153,7 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
     }
   }
   __syncthreads();
-  for (int e = tid; e < rows * (kHeadDim / 4); e += kAttnThreads) {
+  for (int e = tid; e < rows * (kHeadDim / 4); e += W * 32) {
     const int row = e / (kHeadDim / 4);
     const int d = (e % (kHeadDim / 4)) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -183,9 +185,17 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
   }
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams p) {
-  using S = Smem<MT>;
+// Register caps: 4-warp CTAs fit 3 per SM (170 registers), wider ones 2.
+constexpr int attn_min_blocks(int warps) { return warps <= 4 ? 3 : 2; }
+
+template <int MT, int WN>
+__global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_persistent(const AttnParams p) {
+  constexpr int W = MT * WN;                 // warps: WN per 16-row query tile
+  constexpr int kThreads = W * 32;
+  constexpr int NT = kTile / (8 * WN);       // 8-token MMA tiles of S per warp
+  constexpr int ND = kHeadDim / (8 * WN);    // 8-dim MMA tiles of O per warp
+  static_assert(NT >= 1 && ND >= 2 && ND % 2 == 0, "warps per row tile");
+  using S = Smem<MT, W>;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sK = smem_addr(smem + S::off_k);
   const uint32_t sV = smem_addr(smem + S::off_v);
@@ -195,8 +205,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
   float* red_max = reinterpret_cast<float*>(smem + S::off_rmax);
   float* red_l = reinterpret_cast<float*>(smem + S::off_rl);
   int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + S::off_prefix);
-  __shared__ int s_warp[kAttnWarps];
-  __shared__ int s_misc[2];
+  __shared__ int s_warp[W];
+  __shared__ int s_misc[3];   // unit index, "merge here" flag, "unit has a bad row id" flag
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = lane >> 2, tq = lane & 3;
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
 
   // ---- per-request unit counts and their prefix (each CTA computes its own copy) ----
   {
-    const int per = (B + kAttnThreads - 1) / kAttnThreads;
+    const int per = (B + kThreads - 1) / kThreads;
     int sum = 0;
     for (int i = 0; i < per; ++i) {
       const int r = tid * per + i;
@@ -217,7 +227,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
       sum += units;
     }
     int total;
-    int run = block_exclusive_scan<kAttnThreads>(sum, s_warp, &total);
+    int run = block_exclusive_scan<kThreads>(sum, s_warp, &total);
     for (int i = 0; i < per; ++i) {
       const int r = tid * per + i;
       if (r < B) {
@@ -236,7 +246,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
 
   for (;;) {
     __syncthreads();
-    if (tid == 0) s_misc[0] = int(atomicAdd(p.q_next, 1u));
+    if (tid == 0) {
+      s_misc[0] = int(atomicAdd(p.q_next, 1u));
+      s_misc[2] = 0;
+    }
     __syncthreads();
     const long long u = s_misc[0];
     if (u >= total) break;
@@ -259,7 +272,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
     const int G = p.group;
 
     // ---- 1. row ids (page * Hkv + h) * 16 + slot of every entry of the chunk ----
-    for (int i = tid; i < ntok; i += kAttnThreads) {
+    for (int i = tid; i < ntok; i += kThreads) {
       const int e = tok0 + i;
       int pos;
       int bad = 0;
@@ -277,12 +290,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
         if (pg < 0 || pg >= p.num_pages) bad = SSPEC_DEVERR_PAGE_OOB;
         else rid = (pg * p.hkv + h) * kPage + (pos & (kPage - 1));
       }
-      if (bad) atomicOr(p.err, bad);
+      if (bad) {
+        atomicOr(p.err, bad);
+        s_misc[2] = 1;
+      }
       s_row[i] = rid;
     }
 
     // ---- 2. query rows of this kv head into shared memory (zero padded) ----
-    for (int e = tid; e < MT * 16 * 16; e += kAttnThreads) {
+    for (int e = tid; e < MT * 16 * 16; e += kThreads) {
       const int row = e >> 4, ch = e & 15;
       const bool valid = row < q.rows;
       const uint16_t* src = p.q;
@@ -295,14 +311,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
     }
     cp_async_commit();
     __syncthreads();
+    const bool unit_clean = s_misc[2] == 0;
+    // the last position every query row of the unit may see (drafts see their whole list)
+    const int vis_all = q.verify ? q.L - p.nq : INT_MAX;
 
     const int ntiles = (ntok + kTile - 1) / kTile;
     auto load_tile = [&](int t, int st) {
       const uint32_t kb = sK + st * kTile * kRowBytes;
       const uint32_t vb = sV + st * kTile * kRowBytes;
 #pragma unroll
-      for (int m = 0; m < (kTile * 16) / kAttnThreads; ++m) {
-        const int e = tid + m * kAttnThreads;
+      for (int m = 0; m < (kTile * 16 + kThreads - 1) / kThreads; ++m) {
+        const int e = tid + m * kThreads;
+        if ((kTile * 16) % kThreads != 0 && e >= kTile * 16) break;
         const int row = e >> 4, ch = e & 15;
         const int i = t * kTile + row;
         const int rid = (i < ntok) ? s_row[i] : -1;
@@ -317,30 +337,36 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
       cp_async_commit();
     }
 
-    float m_run[MT][2], l_run[MT][2];
-    float o[MT][4][4];
+    // Warp (mg, ng) owns query-row tile mg (rows 16 mg .. 16 mg + 15) and, of every
+    // 64-token tile, tokens 8 NT ng .. for S = Q K^T and output dims 8 ND ng .. for
+    // O += P V.  Warps of a row tile past the unit's rows only load and synchronise.
+    const int mg = MT == 1 ? 0 : warp / WN, ng = warp - mg * WN;
+    const bool active = MT == 1 || mg < mt_used;
+    // l_run keeps one running row sum per 8-token column group of the tile, so the
+    // order in which a row's sum is formed does not depend on the warp layout
+    float m_run[2], l_run[NT][2];
+    float o[ND][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
+    for (int hh = 0; hh < 2; ++hh) {
+      m_run[hh] = -INFINITY;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) { m_run[mt][hh] = -INFINITY; l_run[mt][hh] = 0.f; }
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[mt][n][i] = 0.f;
+      for (int nt = 0; nt < NT; ++nt) l_run[nt][hh] = 0.f;
     }
+#pragma unroll
+    for (int n = 0; n < ND; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
     const bool dump = q.verify && p.logits != nullptr;
     // per query row of this thread: last visible position (verification: query j sees
     // positions <= L - nq + j; a draft sees its whole list) and its logit row in the dump
-    int vis_lim[MT][2];
-    float* drow[MT][2];
+    int vis_lim[2];
+    float* drow[2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int row = mt * 16 + g8 + hh * 8;
-        vis_lim[mt][hh] = q.verify ? q.L - p.nq + row / G : INT_MAX;
-        drow[mt][hh] = (dump && row < q.rows) ? p.logits + q.loff + (size_t(h) * q.rows + row) * q.L : nullptr;
-      }
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = mg * 16 + g8 + hh * 8;
+      vis_lim[hh] = q.verify ? q.L - p.nq + row / G : INT_MAX;
+      drow[hh] = (dump && row < q.rows) ? p.logits + q.loff + (size_t(h) * q.rows + row) * q.L : nullptr;
+    }
 
     for (int t = 0; t < ntiles; ++t) {
       cp_async_wait<kStages - 2>();
@@ -354,198 +380,200 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
       const uint32_t kb = sK + st * kTile * kRowBytes;
       const uint32_t vb = sV + st * kTile * kRowBytes;
 
-      // ---- S = Q K^T for this warp's 16 tokens ----
-      float sacc[MT][2][4];
+      float sacc[NT][4];
+      if (active) {
+        // ---- S = Q K^T for this warp's row tile and 8 * NT tokens ----
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+          for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sacc[mt][nt][i] = 0.f;
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t bk[NT][4];
 #pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {
-        uint32_t bk[2][4];
+          for (int nt = 0; nt < NT; ++nt)
+            ldsm_x4(kb + swz256(ng * 8 * NT + nt * 8 + (lane & 7), kp * 4 + (lane >> 3)), bk[nt]);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-          ldsm_x4(kb + swz256(warp * 16 + nt * 8 + (lane & 7), kp * 4 + (lane >> 3)), bk[nt]);
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int ks = kp * 2 + e2;
+            uint32_t a[4];
+            ldsm_x4(sQ + swz256(mg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, ks * 2 + (lane >> 4)), a);
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int ks = kp * 2 + e2;
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            if (mt < mt_used) {
-              uint32_t a[4];
-              ldsm_x4(sQ + swz256(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, ks * 2 + (lane >> 4)), a);
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(sacc[mt][nt], a, bk[nt][2 * e2], bk[nt][2 * e2 + 1]);
-            }
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sacc[nt], a, bk[nt][2 * e2], bk[nt][2 * e2 + 1]);
           }
         }
-      }
 
-      // ---- mask, dump, per-row tile maximum ----
-      float rmax[MT][2];
+        // ---- mask, dump, per-row maximum over this warp's tokens ----
+        float rmax[2] = {-INFINITY, -INFINITY};
+        // a tile whose 64 entries all exist and are visible to every row needs no mask
+        const bool interior = unit_clean && (t + 1) * kTile <= ntok && tok0 + (t + 1) * kTile - 1 <= vis_all;
+        if (interior) {
+          const int pbase = tok0 + t * kTile + ng * 8 * NT + tq * 2;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) { rmax[mt][0] = -INFINITY; rmax[mt][1] = -INFINITY; }
+          for (int hh = 0; hh < 2; ++hh) {
+            float* dr = drow[hh] != nullptr ? drow[hh] + pbase : nullptr;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-          const int tok = warp * 16 + nt * 8 + tq * 2 + ii;
-          const int i = t * kTile + tok;
-          const bool valid = i < ntok && s_row[i] >= 0;
-          const int pos = tok0 + i;
+              for (int ii = 0; ii < 2; ++ii) {
+                const float x = sacc[nt][hh * 2 + ii];
+                if (dr != nullptr) dr[nt * 8 + ii] = x * p.sm_scale;
+                const float s2 = x * p.scale_log2;
+                sacc[nt][hh * 2 + ii] = s2;
+                rmax[hh] = fmaxf(rmax[hh], s2);
+              }
+          }
+        } else {
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
+          for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const float x = sacc[mt][nt][hh * 2 + ii];
-              const bool vis = valid && pos <= vis_lim[mt][hh];
-              if (drow[mt][hh] != nullptr && i < ntok) drow[mt][hh][pos] = vis ? x * p.sm_scale : -INFINITY;
-              const float s2 = vis ? x * p.scale_log2 : -INFINITY;
-              sacc[mt][nt][hh * 2 + ii] = s2;
-              rmax[mt][hh] = fmaxf(rmax[mt][hh], s2);
+            for (int ii = 0; ii < 2; ++ii) {
+              const int tok = ng * 8 * NT + nt * 8 + tq * 2 + ii;
+              const int i = t * kTile + tok;
+              const bool valid = i < ntok && s_row[i] >= 0;
+              const int pos = tok0 + i;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float x = sacc[nt][hh * 2 + ii];
+                const bool vis = valid && pos <= vis_lim[hh];
+                if (drow[hh] != nullptr && i < ntok) drow[hh][pos] = vis ? x * p.sm_scale : -INFINITY;
+                const float s2 = vis ? x * p.scale_log2 : -INFINITY;
+                sacc[nt][hh * 2 + ii] = s2;
+                rmax[hh] = fmaxf(rmax[hh], s2);
+              }
             }
           }
         }
-      }
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          float v = rmax[mt][hh];
+          float v = rmax[hh];
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-          if (tq == 0) red_max[warp * MT * 16 + mt * 16 + g8 + hh * 8] = v;
+          if (tq == 0) red_max[warp * 16 + g8 + hh * 8] = v;
         }
+      }
       __syncthreads();
 
-      // ---- new running max, probabilities, rescale ----
-      float alpha[MT][2], muse[MT][2];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      if (active) {
+        // ---- running max over the row tile's warps, probabilities, rescale ----
+        // The reference maximum of a row moves only when the tile's maximum exceeds it
+        // by more than kLazyMax (log2 units), so probabilities stay below 2^kLazyMax and
+        // most tiles need no rescale; the warp skips the rescale when no row moved
+        // (the factor is then exactly 1).
+        float alpha[2], muse[2];
+        bool moved = false;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int row = mt * 16 + g8 + hh * 8;
-          float tmax = red_max[row];
+          const int r16 = g8 + hh * 8;
+          float tmax = red_max[mg * WN * 16 + r16];
 #pragma unroll
-          for (int w = 1; w < kAttnWarps; ++w) tmax = fmaxf(tmax, red_max[w * MT * 16 + row]);
-          const float m_new = fmaxf(m_run[mt][hh], tmax);
-          muse[mt][hh] = (m_new == -INFINITY) ? 0.f : m_new;
-          alpha[mt][hh] = exp2f(m_run[mt][hh] - muse[mt][hh]);
-          m_run[mt][hh] = m_new;
+          for (int w = 1; w < WN; ++w) tmax = fmaxf(tmax, red_max[(mg * WN + w) * 16 + r16]);
+          const bool move = tmax > m_run[hh] + kLazyMax;
+          alpha[hh] = move ? exp2f(m_run[hh] - tmax) : 1.f;
+          m_run[hh] = move ? tmax : m_run[hh];
+          muse[hh] = (m_run[hh] == -INFINITY) ? 0.f : m_run[hh];
+          moved |= move;
         }
+        const bool rescale = __any_sync(0xffffffffu, moved);
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        float ls[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
+          float ls[2] = {0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float pv = exp2f(sacc[mt][nt][i] - muse[mt][i >> 1]);
-            sacc[mt][nt][i] = pv;
+            const float pv = exp2f(sacc[nt][i] - muse[i >> 1]);
+            sacc[nt][i] = pv;
             ls[i >> 1] += pv;
           }
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) l_run[mt][hh] = l_run[mt][hh] * alpha[mt][hh] + ls[hh];
-        if (mt < mt_used) {
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int row = mt * 16 + g8 + hh * 8;
-              st_shared_u32(sP + swz128(row, warp * 2 + nt) + tq * 4,
-                            pack_bf16x2(sacc[mt][nt][hh * 2], sacc[mt][nt][hh * 2 + 1]));
-            }
+          for (int hh = 0; hh < 2; ++hh) l_run[nt][hh] = l_run[nt][hh] * alpha[hh] + ls[hh];
         }
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[mt][n][i] *= alpha[mt][i >> 1];
+          for (int hh = 0; hh < 2; ++hh)
+            st_shared_u32(sP + swz128(mg * 16 + g8 + hh * 8, ng * NT + nt) + tq * 4,
+                          pack_bf16x2(sacc[nt][hh * 2], sacc[nt][hh * 2 + 1]));
+        if (rescale) {
+#pragma unroll
+          for (int n = 0; n < ND; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[n][i] *= alpha[i >> 1];
+        }
       }
       __syncthreads();
 
-      // ---- O += P V for this warp's 32 output dims ----
+      if (active) {
+        // ---- O += P V for this warp's row tile and 8 * ND output dims ----
 #pragma unroll
-      for (int kt = 0; kt < kTile / 16; ++kt) {
-        uint32_t bv[2][4];
+        for (int kt = 0; kt < kTile / 16; ++kt) {
+          uint32_t bv[ND / 2][4];
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
-          ldsm_x4_trans(vb + swz256(kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, warp * 4 + half * 2 + (lane >> 4)),
-                        bv[half]);
+          for (int half = 0; half < ND / 2; ++half)
+            ldsm_x4_trans(vb + swz256(kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, ng * ND + half * 2 + (lane >> 4)),
+                          bv[half]);
+          uint32_t a[4];
+          ldsm_x4(sP + swz128(mg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kt * 2 + (lane >> 4)), a);
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          if (mt < mt_used) {
-            uint32_t a[4];
-            ldsm_x4(sP + swz128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kt * 2 + (lane >> 4)), a);
-#pragma unroll
-            for (int n = 0; n < 4; ++n) mma_bf16_16816(o[mt][n], a, bv[n >> 1][(n & 1) * 2], bv[n >> 1][(n & 1) * 2 + 1]);
-          }
+          for (int n = 0; n < ND; ++n) mma_bf16_16816(o[n], a, bv[n >> 1][(n & 1) * 2], bv[n >> 1][(n & 1) * 2 + 1]);
         }
       }
     }
 
-    // ---- epilogue: full row sums ----
+    // ---- epilogue: full row sums (column groups added in a fixed order) ----
+    if (active) {
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float v = l_run[mt][hh];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        if (tq == 0) red_l[warp * MT * 16 + mt * 16 + g8 + hh * 8] = v;
-      }
+        for (int hh = 0; hh < 2; ++hh) {
+          float v = l_run[nt][hh];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          if (tq == 0) red_l[(ng * NT + nt) * MT * 16 + mg * 16 + g8 + hh * 8] = v;
+        }
+    }
     __syncthreads();
-    float ltot[MT][2];
+    float ltot[2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = mg * 16 + g8 + hh * 8;
+      float s = 0.f;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int row = mt * 16 + g8 + hh * 8;
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) s += red_l[w * MT * 16 + row];
-        ltot[mt][hh] = s;
-      }
+      for (int cg = 0; cg < kTile / 8; ++cg) s += red_l[cg * MT * 16 + row];
+      ltot[hh] = s;
+    }
 
     if (nch == 1) {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = mg * 16 + g8 + hh * 8;
+        if (active && row < q.rows) {
+          const long long orow = q.verify ? q.qbase + row / G : q.qbase;
+          const int hq = h * G + (q.verify ? row % G : row);
+          const float inv = 1.f / ltot[hh];
+          uint16_t* dst = p.out + (size_t(orow) * p.hq + hq) * kHeadDim + ng * 8 * ND + tq * 2;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int row = mt * 16 + g8 + hh * 8;
-          if (mt < mt_used && row < q.rows) {
-            const long long orow = q.verify ? q.qbase + row / G : q.qbase;
-            const int hq = h * G + (q.verify ? row % G : row);
-            const float inv = 1.f / ltot[mt][hh];
-            uint16_t* dst = p.out + (size_t(orow) * p.hq + hq) * kHeadDim + warp * 32 + tq * 2;
-#pragma unroll
-            for (int n = 0; n < 4; ++n)
-              *reinterpret_cast<uint32_t*>(dst + n * 8) =
-                  pack_bf16x2(o[mt][n][hh * 2] * inv, o[mt][n][hh * 2 + 1] * inv);
-            if (warp == 0 && tq == 0)
-              p.lse[size_t(orow) * p.hq + hq] = (m_run[mt][hh] + log2f(ltot[mt][hh])) * kLn2;
-          }
+          for (int n = 0; n < ND; ++n)
+            *reinterpret_cast<uint32_t*>(dst + n * 8) = pack_bf16x2(o[n][hh * 2] * inv, o[n][hh * 2 + 1] * inv);
+          if (ng == 0 && tq == 0) p.lse[size_t(orow) * p.hq + hq] = (m_run[hh] + log2f(ltot[hh])) * kLn2;
         }
+      }
     } else {
       const size_t ustride = size_t(p.unit_stride);
       float* part = p.partials + size_t(u) * ustride;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = mg * 16 + g8 + hh * 8;
+        if (active && row < q.rows) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int row = mt * 16 + g8 + hh * 8;
-          if (mt < mt_used && row < q.rows) {
-#pragma unroll
-            for (int n = 0; n < 4; ++n)
-              *reinterpret_cast<float2*>(part + row * kHeadDim + warp * 32 + n * 8 + tq * 2) =
-                  make_float2(o[mt][n][hh * 2], o[mt][n][hh * 2 + 1]);
-            if (warp == 0 && tq == 0) {
-              part[size_t(p.rows_max) * kHeadDim + row] = m_run[mt][hh];
-              part[size_t(p.rows_max) * (kHeadDim + 1) + row] = ltot[mt][hh];
-            }
+          for (int n = 0; n < ND; ++n)
+            *reinterpret_cast<float2*>(part + row * kHeadDim + ng * 8 * ND + n * 8 + tq * 2) =
+                make_float2(o[n][hh * 2], o[n][hh * 2 + 1]);
+          if (ng == 0 && tq == 0) {
+            part[size_t(p.rows_max) * kHeadDim + row] = m_run[hh];
+            part[size_t(p.rows_max) * (kHeadDim + 1) + row] = ltot[hh];
           }
         }
+      }
       __syncthreads();
       if (tid == 0) {
         __threadfence();
@@ -555,7 +583,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
       __syncthreads();
       if (s_misc[1]) {
         __threadfence();
-        merge_partials<MT>(p, q, h, u - c, nch, reinterpret_cast<float*>(smem + S::off_k));
+        merge_partials<MT, W>(p, q, h, u - c, nch, reinterpret_cast<float*>(smem + S::off_k));
         if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
       }
     }
@@ -572,18 +600,19 @@ __global__ void __launch_bounds__(kAttnThreads) attn_persistent(const AttnParams
   }
 }
 
-template <int MT>
+template <int MT, int WN>
 cudaError_t launch_mt(const AttnParams& p, cudaStream_t stream) {
-  const size_t smem = Smem<MT>::bytes(p.batch);
-  cudaError_t e = cudaFuncSetAttribute(attn_persistent<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(Smem<MT>::bytes(SSPEC_MAX_BATCH)));
+  constexpr int W = MT * WN;
+  const size_t smem = Smem<MT, W>::bytes(p.batch);
+  cudaError_t e = cudaFuncSetAttribute(attn_persistent<MT, WN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(Smem<MT, W>::bytes(SSPEC_MAX_BATCH)));
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_persistent<MT>, kAttnThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_persistent<MT, WN>, W * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int grid = device_sm_count() * per_sm;
-  attn_persistent<MT><<<grid, kAttnThreads, smem, stream>>>(p);
+  attn_persistent<MT, WN><<<grid, W * 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -592,10 +621,10 @@ cudaError_t launch_mt(const AttnParams& p, cudaStream_t stream) {
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
   const int mt = (p.rows_max + 15) / 16;
   switch (mt) {
-    case 1: return launch_mt<1>(p, stream);
-    case 2: return launch_mt<2>(p, stream);
-    case 3: return launch_mt<3>(p, stream);
-    case 4: return launch_mt<4>(p, stream);
+    case 1: return launch_mt<1, 4>(p, stream);
+    case 2: return launch_mt<2, 4>(p, stream);
+    case 3: return launch_mt<3, 2>(p, stream);
+    case 4: return launch_mt<4, 2>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -21,8 +21,8 @@ constexpr int kChunk = 768;
 constexpr int kMaxChunks = 256;    // per (request, kv head): bounds the merge scratch
 constexpr int kTile = 64;          // tokens per pipeline stage
 constexpr int kStages = 2;         // cp.async pipeline depth (two CTAs per SM for every shape)
-constexpr int kAttnWarps = 4;
-constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kAttnWarps = 4;      // warps per CTA when the query rows fit one 16-row MMA tile
+constexpr int kAttnWarpsWide = 8;  // warps per CTA for 2-4 row tiles (verification with k*G > 16)
 
 // ---- selection work decomposition ----------------------------------------------------
 constexpr int kSelBlock = 4096;    // tokens averaged per unit
