@@ -109,7 +109,6 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
   p.hkv = shape->num_kv_heads;
   p.group = G;
   p.sm_scale = shape->sm_scale;
-  p.scale_log2 = shape->sm_scale * 1.4426950408889634f;
   p.batch = batch;
   p.nq = any_verify ? nq : 1;
   p.mode = mode;

@@ -32,6 +32,7 @@ namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyMax = 8.f;   // log2 of the largest unnormalised probability
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRowBytes = kHeadDim * 2;  // one token row of one head: 256 B
 
 struct Req {
@@ -111,6 +112,11 @@ struct Smem {
 // byte offset of 16-byte chunk `ch` of row `row` in a 256-byte-row swizzled tile
 __device__ __forceinline__ uint32_t swz256(int row, int ch) {
   return uint32_t(row * kRowBytes + ((ch ^ (row & 7)) << 4));
+}
+// byte offset of logit (row, col) in the 256-byte-row dump staging tile; col is even
+// for the paired writes, and the XOR keeps a warp's eight rows on distinct banks
+__device__ __forceinline__ uint32_t dump_stage_off(int row, int col) {
+  return uint32_t(row * (kTile * 4) + ((col ^ ((row & 3) << 3)) << 2));
 }
 // same for the 128-byte rows of the probability tile
 __device__ __forceinline__ uint32_t swz128(int row, int ch) {
@@ -358,15 +364,12 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
     const bool dump = q.verify && p.logits != nullptr;
     // per query row of this thread: last visible position (verification: query j sees
-    // positions <= L - nq + j; a draft sees its whole list) and its logit row in the dump
+    // positions <= L - nq + j; a draft sees its whole list)
     int vis_lim[2];
-    float* drow[2];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int row = mg * 16 + g8 + hh * 8;
-      vis_lim[hh] = q.verify ? q.L - p.nq + row / G : INT_MAX;
-      drow[hh] = (dump && row < q.rows) ? p.logits + q.loff + (size_t(h) * q.rows + row) * q.L : nullptr;
-    }
+    for (int hh = 0; hh < 2; ++hh) vis_lim[hh] = q.verify ? q.L - p.nq + (mg * 16 + g8 + hh * 8) / G : INT_MAX;
+    // the unit's first logit of row 0 of this kv head in the dump
+    float* dump_base = dump ? p.logits + q.loff + size_t(h) * q.rows * q.L + tok0 : nullptr;
 
     for (int t = 0; t < ntiles; ++t) {
       cp_async_wait<kStages - 2>();
@@ -403,43 +406,34 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
           }
         }
 
-        // ---- mask, dump, per-row maximum over this warp's tokens ----
+        // ---- mask: scaled logits (natural units, -inf where not visible) and the
+        // per-row maximum over this warp's tokens ----
         float rmax[2] = {-INFINITY, -INFINITY};
         // a tile whose 64 entries all exist and are visible to every row needs no mask
         const bool interior = unit_clean && (t + 1) * kTile <= ntok && tok0 + (t + 1) * kTile - 1 <= vis_all;
         if (interior) {
-          const int pbase = tok0 + t * kTile + ng * 8 * NT + tq * 2;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float* dr = drow[hh] != nullptr ? drow[hh] + pbase : nullptr;
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int ii = 0; ii < 2; ++ii) {
-                const float x = sacc[nt][hh * 2 + ii];
-                if (dr != nullptr) dr[nt * 8 + ii] = x * p.sm_scale;
-                const float s2 = x * p.scale_log2;
-                sacc[nt][hh * 2 + ii] = s2;
-                rmax[hh] = fmaxf(rmax[hh], s2);
-              }
-          }
+            for (int i = 0; i < 4; ++i) {
+              const float d = sacc[nt][i] * p.sm_scale;
+              sacc[nt][i] = d;
+              rmax[i >> 1] = fmaxf(rmax[i >> 1], d);
+            }
         } else {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int ii = 0; ii < 2; ++ii) {
-              const int tok = ng * 8 * NT + nt * 8 + tq * 2 + ii;
-              const int i = t * kTile + tok;
+              const int i = t * kTile + ng * 8 * NT + nt * 8 + tq * 2 + ii;
               const bool valid = i < ntok && s_row[i] >= 0;
               const int pos = tok0 + i;
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
-                const float x = sacc[nt][hh * 2 + ii];
                 const bool vis = valid && pos <= vis_lim[hh];
-                if (drow[hh] != nullptr && i < ntok) drow[hh][pos] = vis ? x * p.sm_scale : -INFINITY;
-                const float s2 = vis ? x * p.scale_log2 : -INFINITY;
-                sacc[nt][hh * 2 + ii] = s2;
-                rmax[hh] = fmaxf(rmax[hh], s2);
+                const float d = vis ? sacc[nt][hh * 2 + ii] * p.sm_scale : -INFINITY;
+                sacc[nt][hh * 2 + ii] = d;
+                rmax[hh] = fmaxf(rmax[hh], d);
               }
             }
           }
@@ -449,12 +443,24 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
           float v = rmax[hh];
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-          if (tq == 0) red_max[warp * 16 + g8 + hh * 8] = v;
+          if (tq == 0) red_max[warp * 16 + g8 + hh * 8] = v * kLog2e;   // log2 units
         }
       }
       __syncthreads();
 
       if (active) {
+        // ---- the logit dump is staged in this tile's K stage (free once every warp
+        // has finished Q K^T) and written out row by row after the next barrier ----
+        if (dump) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int row = mg * 16 + g8 + hh * 8;
+              const int col = ng * 8 * NT + nt * 8 + tq * 2;
+              st_shared_f32x2(kb + dump_stage_off(row, col), sacc[nt][hh * 2], sacc[nt][hh * 2 + 1]);
+            }
+        }
         // ---- running max over the row tile's warps, probabilities, rescale ----
         // The reference maximum of a row moves only when the tile's maximum exceeds it
         // by more than kLazyMax (log2 units), so probabilities stay below 2^kLazyMax and
@@ -480,7 +486,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
           float ls[2] = {0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float pv = exp2f(sacc[nt][i] - muse[i >> 1]);
+            const float pv = exp2f(fmaf(sacc[nt][i], kLog2e, -muse[i >> 1]));
             sacc[nt][i] = pv;
             ls[i >> 1] += pv;
           }
@@ -501,6 +507,19 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
         }
       }
       __syncthreads();
+
+      // ---- write the staged logits: each warp stores whole 64-entry row segments ----
+      if (dump) {
+        const int cols = min(kTile, ntok - t * kTile);
+        for (int row = warp; row < q.rows; row += W) {
+          float* dst = dump_base + size_t(row) * q.L + t * kTile;
+#pragma unroll
+          for (int c0 = 0; c0 < kTile; c0 += 32) {
+            const int col = c0 + lane;
+            if (col < cols) dst[col] = ld_shared_f32(kb + dump_stage_off(row, col));
+          }
+        }
+      }
 
       if (active) {
         // ---- O += P V for this warp's row tile and 8 * ND output dims ----

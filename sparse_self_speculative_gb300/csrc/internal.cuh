@@ -73,7 +73,6 @@ struct AttnParams {
   int num_pages;
   int hq, hkv, group;
   float sm_scale;     // natural units
-  float scale_log2;   // sm_scale * log2(e)
   int batch;
   int nq;             // verification query rows per request
   int mode;
