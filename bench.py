@@ -80,12 +80,19 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.01)   # the first sample takes a moment; the timed region starts after it
         except Exception:
             self.proc = None
         return self
+
+    def mark(self) -> int:
+        """Number of samples received so far (brackets the timed region)."""
+        return len(self.lines)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -99,10 +106,14 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, lo: int = 0, hi: int = None):
+        """Median SM clock, max clock and throttle reasons of samples lo..hi (the timed
+        region); if none arrived inside it, the first sample after its start."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        hi = len(self.lines) if hi is None else hi
+        window = self.lines[lo:hi] if hi > lo else self.lines[lo:lo + 1]
+        for ln in window:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -239,6 +250,7 @@ def run_ours(args, world, rank, local):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    clk_lo = clk.mark()
     start.record(stream)
     for i in range(args.steps):
         ev_f0[i].record(stream)
@@ -248,6 +260,7 @@ def run_ours(args, world, rank, local):
         ev_s1[i].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
+    clk_hi = clk.mark()
     clk.__exit__()
     barrier(world)
     total_ms = start.elapsed_time(stop)
@@ -314,7 +327,7 @@ def run_ours(args, world, rank, local):
                      "kv_gbs": kv_gbs, "kv_frac": kv_gbs / peak},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(clk_lo, clk_hi),
         "bytes_per_step": {"kv": acc["kv_bytes"], "fused_total": acc["fused_bytes"], "select": acc["select_bytes"]},
     }
     if rank == 0 and not args.no_cpu_baseline:
