@@ -228,6 +228,38 @@ int sspec_fused_step(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t
                      size_t ws_bytes, sspec_stream_t stream);
 
 /*
+ * sspec_fused_step plus pillar selection of its verifying requests, in the same
+ * single persistent launch.  This entry point has no counterpart on the pages:
+ * the pages run selection right after verification and call it overhead-free;
+ * here it runs inside the verification launch, so a head's logit dump is read
+ * back while it is still in L2.
+ *
+ * Inputs and outputs are those of sspec_fused_step, and afterwards every
+ * verifying request holds exactly what sspec_select_pillars (nq = k, q_off as
+ * given) writes for it:
+ *   s           sparsity in (0, 1]; K = max(1, min(L, floor((double)s * L)))
+ *   avg_scores  device fp32, required: averages of request r start at element
+ *               logit_off[r] / (k * G), laid out [Hkv][seq_len]
+ *   idx         device int32: drafting requests' pillars are read; verifying
+ *               requests' rows receive their new pillars (Hkv rows of
+ *               (idx_off[r+1] - idx_off[r]) / Hkv entries, the first K used)
+ *   nsel        device int32 [batch]: read for drafting requests, set to K for
+ *               verifying requests
+ * A drafting request's pillars are read before any verifying request's are
+ * written only in the sense that the two sets of rows are disjoint: a request
+ * either drafts or verifies in one call.  Requests whose idx rows are too short
+ * for K are skipped by the selection and reported with SSPEC_DEVERR_RANGE.
+ * Device waits are bounded (2 s); a wait that runs out sets SSPEC_DEVERR_TIMEOUT.
+ */
+int sspec_fused_step_select(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
+                            int32_t k, const int32_t* bucket, int32_t verify_bucket, const void* q,
+                            const int64_t* q_off, const int32_t* seq_lens, const int32_t* sel_lens,
+                            int32_t* idx, const int64_t* idx_off, int32_t* nsel, float s,
+                            float* avg_scores, void* out, float* lse, float* logits,
+                            const int64_t* logit_off, void* workspace, size_t ws_bytes,
+                            sspec_stream_t stream);
+
+/*
  * Greedy least-loaded bucket assignment (Unified batch scheduler: new requests
  * go to the least-loaded of the k+1 buckets; paper Sec. 4.2, Fig. 8).
  * Host only.  The load of a bucket is its request count; requests are placed in

@@ -62,6 +62,8 @@ _SIGS = {
                                                ctypes.c_size_t, _P]),
     "sspec_fused_step": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P, _P, ctypes.c_size_t, _P]),
+    "sspec_fused_step_select": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                               ctypes.c_float, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "sspec_assign_buckets": (ctypes.c_int, [_I32, _P, _I32, _P]),
     "sspec_error_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -163,6 +165,16 @@ def sspec_fused_step(shape, kv, batch, k, bucket, verify_bucket, q, q_off, seq_l
     _check("sspec_fused_step", rc)
 
 
+def sspec_fused_step_select(shape, kv, batch, k, bucket, verify_bucket, q, q_off, seq_lens, sel_lens, idx,
+                            idx_off, nsel, s, avg_scores, out, lse, logits, logit_off, workspace, stream=None):
+    rc = lib().sspec_fused_step_select(ctypes.byref(shape), ctypes.byref(kv), batch, k, _ptr(bucket),
+                                       verify_bucket, _ptr(q), _ptr(q_off), _ptr(seq_lens), _ptr(sel_lens),
+                                       _ptr(idx), _ptr(idx_off), _ptr(nsel), float(s), _ptr(avg_scores),
+                                       _ptr(out), _ptr(lse), _ptr(logits), _ptr(logit_off), _ptr(workspace),
+                                       _nbytes(workspace), _stream(stream))
+    _check("sspec_fused_step_select", rc)
+
+
 def sspec_assign_buckets(k: int, counts, n_new: int):
     """Host call; ``counts`` is a list of k+1 ints.  Returns (buckets, new counts)."""
     c = (ctypes.c_int32 * (k + 1))(*[int(x) for x in counts])
@@ -181,5 +193,5 @@ def _nbytes(t):
 __all__ = [
     "SspecShape", "SspecPagedKV", "SspecError", "lib", "make_shape", "make_kv", "error_string",
     "sspec_workspace_size", "sspec_verify_attn", "sspec_select_pillars", "sspec_sparse_draft_attn",
-    "sspec_fused_step", "sspec_assign_buckets", "header_functions",
+    "sspec_fused_step", "sspec_fused_step_select", "sspec_assign_buckets", "header_functions",
 ]

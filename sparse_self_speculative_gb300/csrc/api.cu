@@ -52,6 +52,7 @@ struct Ws {
   int32_t* attn_cnt;
   int32_t* sel_cnt;
   uint32_t* sel_hist;
+  unsigned long long* avg_slots;
   uint8_t* region;
   size_t region_bytes;
 };
@@ -66,6 +67,7 @@ int carve(void* workspace, size_t ws_bytes, int batch, int hkv, Ws& w) {
   w.attn_cnt = reinterpret_cast<int32_t*>(b + kWsHeaderBytes);
   w.sel_cnt = reinterpret_cast<int32_t*>(b + kWsHeaderBytes + ws_counter_bytes(batch, hkv));
   w.sel_hist = reinterpret_cast<uint32_t*>(b + kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv));
+  w.avg_slots = reinterpret_cast<unsigned long long*>(b + ws_avg_slot_offset(batch, hkv));
   w.region = b + off;
   w.region_bytes = ws_bytes - off;
   return SSPEC_OK;
@@ -76,7 +78,8 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
                   const int64_t* q_off, const int32_t* seq_lens, const int32_t* sel_lens,
                   const int32_t* idx, const int64_t* idx_off, const int32_t* nsel, void* out,
                   float* lse, float* logits, const int64_t* logit_off, void* workspace,
-                  size_t ws_bytes, sspec_stream_t stream) {
+                  size_t ws_bytes, sspec_stream_t stream, float sel_s = 0.f, float* sel_scores = nullptr,
+                  int32_t* sel_idx = nullptr, int32_t* sel_nsel = nullptr) {
   int rc = check_shape(shape);
   if (rc) return rc;
   if ((rc = check_kv(kv))) return rc;
@@ -134,6 +137,17 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
   if (p.rows_max < G) p.rows_max = G;
   p.unit_stride = (long long)unit_partial_floats(p.rows_max);
   p.unit_capacity = (long long)(w.region_bytes / unit_partial_bytes(p.rows_max));
+  if (sel_scores) {
+    p.sel_s = sel_s;
+    p.sel_scores = sel_scores;
+    p.sel_idx = sel_idx;
+    p.sel_nsel = sel_nsel;
+    p.sel_cnt = w.sel_cnt;
+    p.sel_hist = w.sel_hist;
+    p.avg_slots = w.avg_slots;
+    p.avg_reserve = &w.hdr->avg_reserve;
+    p.avg_head = &w.hdr->avg_head;
+  }
   return launch_attention(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSPEC_OK
                                                                                      : SSPEC_ERR_CUDA;
 }
@@ -179,6 +193,20 @@ int sspec_fused_step(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t
   if (k < 1 || verify_bucket < 0 || verify_bucket > k) return SSPEC_ERR_INVALID_ARG;
   return run_attention(shape, kv, batch, k, kByBucket, bucket, verify_bucket, q, q_off, seq_lens, sel_lens,
                        idx, idx_off, nsel, out, lse, logits, logit_off, workspace, ws_bytes, stream);
+}
+
+int sspec_fused_step_select(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch, int32_t k,
+                            const int32_t* bucket, int32_t verify_bucket, const void* q, const int64_t* q_off,
+                            const int32_t* seq_lens, const int32_t* sel_lens, int32_t* idx,
+                            const int64_t* idx_off, int32_t* nsel, float s, float* avg_scores, void* out,
+                            float* lse, float* logits, const int64_t* logit_off, void* workspace,
+                            size_t ws_bytes, sspec_stream_t stream) {
+  if (k < 1 || verify_bucket < 0 || verify_bucket > k) return SSPEC_ERR_INVALID_ARG;
+  if (!(s > 0.f && s <= 1.f) || !avg_scores || !logits || !logit_off || !idx || !idx_off || !nsel)
+    return SSPEC_ERR_INVALID_ARG;
+  return run_attention(shape, kv, batch, k, kByBucket, bucket, verify_bucket, q, q_off, seq_lens, sel_lens,
+                       idx, idx_off, nsel, out, lse, logits, logit_off, workspace, ws_bytes, stream, s, avg_scores,
+                       idx, nsel);
 }
 
 int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, float s, const float* logits,

@@ -26,6 +26,7 @@
 
 #include "device_common.cuh"
 #include "internal.cuh"
+#include "topk.cuh"
 
 namespace sspec {
 namespace {
@@ -191,6 +192,173 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
   }
 }
 
+// ---- pillar selection inside the fused step ----------------------------------------
+//
+// When the last chunk of a verifying (request, kv head) completes (its output and LSE
+// are final), that CTA publishes the head's averaging items on a second queue: slots
+// are reserved with an atomic counter and then filled with (request, head, block)
+// descriptors.  CTAs take published averaging items before attention units, so the
+// head's logit dump is read back soon after it was written.  The last averaging item
+// of a head to finish runs its Top-K.  The averages and the pillars are computed
+// exactly as the standalone selection computes them.
+
+constexpr unsigned long long kWaitNs = 2000000000ull;   // bound of every wait: 2 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t ld_volatile(const uint32_t* a) { return *reinterpret_cast<const volatile uint32_t*>(a); }
+
+__device__ __forceinline__ unsigned long long avg_desc(int r, int h, int b) {
+  return (1ull << 63) | ((unsigned long long)r << 40) | ((unsigned long long)h << 32) | (unsigned)b;
+}
+
+// Whether verifying request r takes part in the fused selection; *K gets its pillar count.
+__device__ bool sel_request_ok(const AttnParams& p, int r, const Req& q, int* K, bool report) {
+  *K = sel::pillar_count(p.sel_s, q.L);
+  const long long istride = (p.idx_off[r + 1] - p.idx_off[r]) / p.hkv;
+  const bool ok = q.loff % q.rows == 0 && istride >= *K;
+  if (!ok && report) atomicOr(p.err, SSPEC_DEVERR_RANGE);
+  return ok;
+}
+
+// Next task of the CTA (thread 0): 2 = averaging item (queue slot in *item), 1 =
+// attention unit (*item), 0 = nothing left.  A CTA claims an averaging slot with an
+// atomic add when one looks published, and keeps that claim (*pending) while it takes
+// attention units until the slot's descriptor has been written; with no attention left
+// it waits for its own slot (bounded, with backoff), so waiting CTAs poll distinct
+// addresses.
+__device__ int next_task(const AttnParams& p, long long total, uint32_t total_avg, bool& attn_left,
+                         long long& pending, uint32_t* item) {
+  const bool sel = total_avg > 0;
+  unsigned long long t0 = 0;
+  unsigned sleep_ns = 128;
+  for (;;) {
+    if (sel) {
+      if (pending < 0 && pending != -2 &&
+          (!attn_left || ld_volatile(p.avg_head) < ld_volatile(p.avg_reserve))) {
+        const uint32_t c = atomicAdd(p.avg_head, 1u);
+        pending = c < total_avg ? (long long)c : -2;   // -2: every item is claimed
+      }
+      if (pending >= 0 &&
+          *reinterpret_cast<const volatile unsigned long long*>(p.avg_slots + pending) != 0ull) {
+        *item = uint32_t(pending);
+        pending = -1;
+        return 2;
+      }
+    }
+    if (attn_left) {
+      const uint32_t u = atomicAdd(p.q_next, 1u);
+      if ((long long)u < total) {
+        *item = u;
+        return 1;
+      }
+      attn_left = false;
+      continue;
+    }
+    if (!sel || pending == -2) return 0;
+    // only a claimed, not yet published averaging slot is left: wait for it
+    const unsigned long long now = global_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > kWaitNs) {
+      atomicOr(p.err, SSPEC_DEVERR_TIMEOUT);
+      return 0;
+    }
+    __nanosleep(sleep_ns);
+    sleep_ns = sleep_ns < 8192 ? sleep_ns * 2 : 8192;
+  }
+}
+
+// Publishes the averaging items of (r, h) once its output and LSE are written (all
+// threads call it).
+template <int NT>
+__device__ void publish_avg(const AttnParams& p, int r, int h, int L) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int blk = NT * kAvgPerThread;
+    const int nb = (L + blk - 1) / blk;
+    const uint32_t base = atomicAdd(p.avg_reserve, uint32_t(nb));
+    for (int b = 0; b < nb; ++b)
+      *reinterpret_cast<volatile unsigned long long*>(p.avg_slots + base + b) = avg_desc(r, h, b);
+  }
+}
+
+// One averaging item (queue slot `slot`): averages NT * kAvgPerThread positions of one
+// verifying (request, kv head) from the logit dump and LSE, adds their first radix digit
+// to the head's histogram; the head's last item runs its Top-K.  `ring` is the CTA's
+// K/V staging ring (64 KB, idle between units).
+template <int NT>
+__device__ void avg_item(const AttnParams& p, uint32_t slot, uint8_t* ring, int* s_misc, int* s_warp) {
+  constexpr int kBlk = NT * kAvgPerThread;
+  constexpr int kCand = 6144;
+  constexpr int kAvgRowGroup = 8;   // 64 loads in flight a thread: the attention kernel has the registers
+  static_assert(SSPEC_MAX_ROWS % kAvgRowGroup == 0, "row groups fit s_lse");
+  static_assert(kSelBins * 4 + SSPEC_MAX_ROWS * 4 + 2 * NT * 4 + 2 * kCand * 4 <= 2 * kStages * kTile * kRowBytes,
+                "selection shared memory fits the K/V ring");
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(ring);
+  float* s_lse = reinterpret_cast<float*>(ring + kSelBins * 4);
+  uint32_t* s_gt = reinterpret_cast<uint32_t*>(ring + kSelBins * 4 + SSPEC_MAX_ROWS * 4);
+  uint32_t* s_eq = s_gt + NT;
+  int32_t* s_pos = reinterpret_cast<int32_t*>(s_eq + NT);
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(s_pos + kCand);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    // next_task returns a slot only once its descriptor is written
+    const unsigned long long d = *reinterpret_cast<volatile unsigned long long*>(p.avg_slots + slot);
+    p.avg_slots[slot] = 0ull;   // leave the slot empty for the next launch
+    __threadfence();
+    s_misc[0] = d == 0 ? -1 : int((d >> 40) & 0x7FFFFF);
+    s_misc[1] = int((d >> 32) & 0xFF);
+    s_misc[2] = int(d & 0xFFFFFFFFu);
+  }
+  __syncthreads();
+  const int r = s_misc[0], h = s_misc[1], b = s_misc[2];
+  if (r < 0) return;
+  Req q;
+  load_req(p, r, q, false);
+  int K;
+  sel_request_ok(p, r, q, &K, false);
+  const int G = p.group, L = q.L, rows = q.rows;
+  const int nb = (L + kBlk - 1) / kBlk;
+  for (int i = tid; i < kSelBins; i += NT) s_hist[i] = 0u;
+  if (tid < SSPEC_MAX_ROWS)
+    s_lse[tid] = tid < rows ? __ldcg(p.lse + size_t(q.qbase + tid / G) * p.hq + h * G + tid % G) : 0.f;
+  __syncthreads();
+  float* S = p.sel_scores + q.loff / rows + size_t(h) * L;
+  const int t_end = min(L, (b + 1) * kBlk);
+  for (int t_lo = b * kBlk; t_lo < t_end; t_lo += NT * kAvgPass)
+    sel::average_block<NT, kAvgPass, kAvgRowGroup, false>(p.logits + q.loff + size_t(h) * rows * L, L, rows, s_lse, t_lo,
+                                            min(t_end, t_lo + NT * kAvgPass), S, s_hist);
+  __syncthreads();
+  uint32_t* ghist = p.sel_hist + (size_t(r) * p.hkv + h) * kSelBins;
+  for (int i = tid; i < kSelBins; i += NT) {
+    const uint32_t v = s_hist[i];
+    if (v) atomicAdd(ghist + i, v);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&p.sel_cnt[size_t(r) * p.hkv + h], 1);
+    s_misc[0] = prev == nb - 1;
+  }
+  __syncthreads();
+  if (s_misc[0]) {
+    __threadfence();
+    const long long ibase = p.idx_off[r];
+    const long long istride = (p.idx_off[r + 1] - ibase) / p.hkv;
+    const sel::TopkSmem sm{s_hist, s_gt, s_eq, s_pos, s_key, s_misc, s_warp, kCand};
+    sel::topk_ascending<NT>(S, L, K, ghist, p.sel_idx + ibase + h * istride, sm);
+    if (tid == 0) {
+      p.sel_nsel[r] = K;
+      p.sel_cnt[size_t(r) * p.hkv + h] = 0;
+    }
+  }
+}
+
 // Register caps: 4-warp CTAs fit 3 per SM (170 registers), wider ones 2.
 constexpr int attn_min_blocks(int warps) { return warps <= 4 ? 3 : 2; }
 
@@ -212,25 +380,44 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   float* red_l = reinterpret_cast<float*>(smem + S::off_rl);
   int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + S::off_prefix);
   __shared__ int s_warp[W];
-  __shared__ int s_misc[3];   // unit index, "merge here" flag, "unit has a bad row id" flag
+  __shared__ int s_misc[4];   // task item, "merge here" flag, "unit has a bad row id" flag, task kind
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = lane >> 2, tq = lane & 3;
   const int B = p.batch;
 
-  // ---- per-request unit counts and their prefix (each CTA computes its own copy) ----
-  {
+  // ---- the attention queue holds every verification unit first, then every draft
+  // unit: long units start early, and the selection of verified heads overlaps the
+  // drafts.  s_prefix holds the per-request unit prefix of the phase the CTA is in
+  // (rebuilt once when it reaches the draft units); the first build also counts the
+  // draft units and the averaging items of the fused selection ----
+  uint32_t total_avg = 0;
+  long long n_draft = 0;
+  auto build_prefix = [&](bool verify_phase, bool first) -> long long {
     const int per = (B + kThreads - 1) / kThreads;
-    int sum = 0;
+    int sum = 0, other = 0, avg_sum = 0;
     for (int i = 0; i < per; ++i) {
       const int r = tid * per + i;
       int units = 0;
       if (r < B) {
         Req q;
-        if (load_req(p, r, q, blockIdx.x == 0)) units = ((q.T + kChunk - 1) / kChunk) * p.hkv;
+        if (load_req(p, r, q, first && blockIdx.x == 0)) {
+          const int n = ((q.T + kChunk - 1) / kChunk) * p.hkv;
+          if (q.verify == verify_phase) units = n; else other += n;
+          int K;
+          if (first && p.sel_scores != nullptr && q.verify && sel_request_ok(p, r, q, &K, blockIdx.x == 0))
+            avg_sum += ((q.L + kThreads * kAvgPerThread - 1) / (kThreads * kAvgPerThread)) * p.hkv;
+        }
         s_prefix[r + 1] = units;
       }
       sum += units;
+    }
+    if (first) {
+      int t;
+      block_exclusive_scan<kThreads>(avg_sum, s_warp, &t);
+      total_avg = uint32_t(t);
+      block_exclusive_scan<kThreads>(other, s_warp, &t);
+      n_draft = t;
     }
     int total;
     int run = block_exclusive_scan<kThreads>(sum, s_warp, &total);
@@ -243,34 +430,55 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     }
     if (tid == 0) s_prefix[0] = 0;
     __syncthreads();
-  }
-  long long total = s_prefix[B];
+    return total;
+  };
+  const long long n_verify = build_prefix(true, true);
+  bool draft_phase = false;
+  long long total = n_verify + n_draft;
   if (total > p.unit_capacity) {
     if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, SSPEC_DEVERR_WORKSPACE);
     total = 0;
+    total_avg = 0;
   }
 
+  bool attn_left = true;   // thread 0's view of the attention queue
+  long long pending = -1;  // thread 0's claimed, not yet processed averaging slot
   for (;;) {
     __syncthreads();
     if (tid == 0) {
-      s_misc[0] = int(atomicAdd(p.q_next, 1u));
+      uint32_t item = 0;
+      s_misc[3] = next_task(p, total, total_avg, attn_left, pending, &item);
+      s_misc[0] = int(item);
       s_misc[2] = 0;
     }
     __syncthreads();
-    const long long u = s_misc[0];
-    if (u >= total) break;
+    const int kind = s_misc[3];
+    if (kind == 0) break;
+    if (kind == 2) {
+      avg_item<kThreads>(p, uint32_t(s_misc[0]), smem + S::off_k, s_misc, s_warp);
+      continue;
+    }
+    const long long u = s_misc[0];   // unit index over both phases (names its partial state)
+    long long ul = u;                // index within the phase
+    if (u >= n_verify) {
+      if (!draft_phase) {
+        build_prefix(false, false);
+        draft_phase = true;
+      }
+      ul = u - n_verify;
+    }
 
     // ---- decode the unit ----
     int lo = 0, hi = B;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s_prefix[mid] <= u) lo = mid; else hi = mid;
+      if (s_prefix[mid] <= ul) lo = mid; else hi = mid;
     }
     const int r = lo;
     Req q;
     load_req(p, r, q, false);
     const int nch = (s_prefix[r + 1] - s_prefix[r]) / p.hkv;
-    const int local = int(u - s_prefix[r]);
+    const int local = int(ul - s_prefix[r]);
     const int h = local / nch, c = local % nch;
     const int tok0 = c * kChunk;
     const int ntok = min(q.T - tok0, kChunk);
@@ -576,6 +784,10 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
           if (ng == 0 && tq == 0) p.lse[size_t(orow) * p.hq + hq] = (m_run[hh] + log2f(ltot[hh])) * kLn2;
         }
       }
+      if (total_avg > 0 && q.verify) {
+        int K;
+        if (sel_request_ok(p, r, q, &K, false)) publish_avg<kThreads>(p, r, h, q.L);
+      }
     } else {
       const size_t ustride = size_t(p.unit_stride);
       float* part = p.partials + size_t(u) * ustride;
@@ -604,6 +816,10 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
         __threadfence();
         merge_partials<MT, W>(p, q, h, u - c, nch, reinterpret_cast<float*>(smem + S::off_k));
         if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
+        if (total_avg > 0 && q.verify) {
+          int K;
+          if (sel_request_ok(p, r, q, &K, false)) publish_avg<kThreads>(p, r, h, q.L);
+        }
       }
     }
   }
@@ -615,6 +831,10 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     if (prev == gridDim.x - 1) {
       atomicExch(p.q_next, 0u);
       atomicExch(p.q_done, 0u);
+      if (p.sel_scores != nullptr) {
+        atomicExch(p.avg_reserve, 0u);
+        atomicExch(p.avg_head, 0u);
+      }
     }
   }
 }

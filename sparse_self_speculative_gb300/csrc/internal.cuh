@@ -31,18 +31,36 @@ constexpr int kSelBits1 = 11;      // radix digits of the fp32 keys: bits 31..21
 constexpr int kSelBins = 1 << kSelBits1;
 constexpr int kSelSegment = 16384; // positions per compaction segment
 
+// ---- selection inside the fused step ---------------------------------------------------
+// An averaging item covers kAvgPerThread positions per attention thread (4096 to 8192
+// positions), averaged kAvgPass per thread at a time; a (request, kv head) has at most
+// kMaxAvgItems of them.
+constexpr int kAvgPass = 8;
+constexpr int kAvgPerThread = 4 * kAvgPass;
+constexpr int kMaxAvgItems = (kMaxChunks * kChunk + 4095) / 4096;
+
 // ---- workspace layout ------------------------------------------------------------------
-// [0, 256)        header: error word and the persistent-kernel queue counters
+// [0, 512)        header: error word and the persistent-kernel queue counters (the
+//                 averaging queue's two counters on cache lines of their own)
 // [256, ...)      per (request, kv head) arrival counters: attention, then selection
 //                 per (request, kv head) histograms of the first radix digit (selection)
+//                 averaging-item queue slots of the fused step (8 bytes each)
 // [region, end)   attention partial states, or the averaged scores of selection
+// Everything before the region must be zero before the first call; every launch
+// leaves it zero.
 struct WsHeader {
   int32_t err;
   int32_t pad0[3];
   uint32_t attn_next, attn_done;
   uint32_t sel_next, sel_done;
+  uint32_t pad1[24];
+  uint32_t avg_reserve;             // fused step: averaging-queue slots reserved by producers
+  uint32_t pad2[31];
+  uint32_t avg_head;                // and claimed by consumers
+  uint32_t pad3[31];
 };
-constexpr size_t kWsHeaderBytes = 256;
+constexpr size_t kWsHeaderBytes = 512;
+static_assert(sizeof(WsHeader) <= kWsHeaderBytes, "workspace header");
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -52,8 +70,14 @@ inline size_t ws_counter_bytes(int batch, int hkv) {
 inline size_t ws_hist_bytes(int batch, int hkv) {
   return size_t(batch) * size_t(hkv) * kSelBins * sizeof(uint32_t);
 }
-inline size_t ws_region_offset(int batch, int hkv) {
+inline size_t ws_avg_slot_bytes(int batch, int hkv) {
+  return align_up(size_t(batch) * size_t(hkv) * kMaxAvgItems * sizeof(unsigned long long), 256);
+}
+inline size_t ws_avg_slot_offset(int batch, int hkv) {
   return kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv) + ws_hist_bytes(batch, hkv);
+}
+inline size_t ws_region_offset(int batch, int hkv) {
+  return ws_avg_slot_offset(batch, hkv) + ws_avg_slot_bytes(batch, hkv);
 }
 // one unit's partial state: O [rows][128] fp32, then m [rows], l [rows]; the stride
 // is padded to 4 floats so every O row starts 16-byte aligned
@@ -98,6 +122,16 @@ struct AttnParams {
   long long unit_capacity;
   int rows_max;               // rows of a partial state
   long long unit_stride;      // floats between consecutive partial states
+  // pillar selection of the verifying requests inside the same launch (sel_scores null: off)
+  float sel_s;
+  float* sel_scores;          // averages of request r at logit_off[r] / (nq * group)
+  int32_t* sel_idx;           // pillars out (the draft requests' rows of the same array are read)
+  int32_t* sel_nsel;
+  int32_t* sel_cnt;           // per (request, kv head) averaging-item arrival counters
+  uint32_t* sel_hist;         // per (request, kv head) first-digit histograms
+  unsigned long long* avg_slots;   // averaging-item queue
+  uint32_t* avg_reserve;
+  uint32_t* avg_head;
 };
 
 struct SelectParams {

@@ -207,6 +207,20 @@ class UnifiedStep:
                             self.d_nsel, self.d_out, self.d_lse, self.d_logits, self.d_logit_off, self.ws,
                             stream)
 
+    def fused_select(self, avg_scores, stream=None):
+        """The fused step with the verifying requests' pillar selection in the same launch."""
+        import sparse_self_speculative_gb300 as ss
+        ss.sspec_fused_step_select(self.shape, self.dkv.kv(), self.wl.batch, self.k, self.d_bucket,
+                                   self.verify_bucket, self.d_q, self.d_q_off, self.d_seq, self.d_sel, self.d_idx,
+                                   self.d_idx_off, self.d_nsel, self.s, avg_scores, self.d_out, self.d_lse,
+                                   self.d_logits, self.d_logit_off, self.ws, stream)
+
+    def score_buffer(self):
+        """Device buffer for the averages of the verifying requests (logit_off / (k*G) layout)."""
+        G = self.wl.num_q_heads // self.wl.num_kv_heads
+        return torch.empty(max(1, int(self.logit_off[-1]) // (self.k * G)), dtype=torch.float32,
+                           device=self.d_q.device)
+
     def select(self, stream=None, avg_scores=None):
         import sparse_self_speculative_gb300 as ss
         ss.sspec_select_pillars(self.shape, self.wl.batch, self.k, self.s, self.d_logits, self.d_logit_off,

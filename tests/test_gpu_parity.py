@@ -358,3 +358,46 @@ def test_device_generator_matches_host():
     for which, t in (("k", a.k), ("v", a.v)):
         host = wl.paged_cache(which)
         np.testing.assert_array_equal(hz.to_bits(t), host)
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (40, 8)])
+def test_fused_select_equals_separate_launches_bitwise(hq, hkv):
+    """Selection inside the fused launch writes exactly what the fused step followed by
+    the standalone selection writes: outputs, LSE, dump, averages, pillars and counts;
+    a second call (queue counters and slots reset by the first) gives the same again."""
+    k, s = 8, 0.05
+    rng = np.random.default_rng(hq + 1000)
+    lens = np.concatenate([[9000, 64, 1025, 3072, 1536, 2049], rng.integers(40, 5000, size=30)]).astype(np.int32)
+    wl = synth.make_workload("fsel", 4242 + hq, hq, hkv, lens, plant="kv_per_head", plant_frac=0.01)
+    import sparse_self_speculative_gb300 as ss
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), len(lens))
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, pillars="synthetic")
+    vr = np.flatnonzero(st.is_verify)
+    assert len(vr) >= 3
+    # reference: two launches
+    st.fused()
+    S_ref = st.score_buffer()
+    st.select(avg_scores=S_ref)
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0
+    ref = dict(out=hz.to_bits(st.d_out).copy(), lse=st.d_lse.cpu().numpy().copy(),
+               logits=st.d_logits.cpu().numpy().copy(), idx=st.d_idx.cpu().numpy().copy(),
+               nsel=st.d_nsel.cpu().numpy().copy(), S=S_ref.cpu().numpy().copy())
+    for call in range(2):
+        # clear what the fused selection must write for the verifying requests
+        for r in vr:
+            st.d_idx[int(st.idx_off[r]):int(st.idx_off[r + 1])] = -7
+        st.d_nsel[torch.from_numpy(vr).cuda()] = -7
+        st.d_out.fill_(0)
+        S = st.score_buffer()
+        S.fill_(float("nan"))
+        st.fused_select(S)
+        torch.cuda.synchronize()
+        assert hz.device_error(st.ws) == 0, f"call {call}"
+        np.testing.assert_array_equal(hz.to_bits(st.d_out), ref["out"])
+        np.testing.assert_array_equal(st.d_lse.cpu().numpy(), ref["lse"])
+        np.testing.assert_array_equal(st.d_logits.cpu().numpy(), ref["logits"])
+        np.testing.assert_array_equal(st.d_idx.cpu().numpy(), ref["idx"])
+        np.testing.assert_array_equal(st.d_nsel.cpu().numpy(), ref["nsel"])
+        np.testing.assert_array_equal(S.cpu().numpy(), ref["S"])
