@@ -37,17 +37,26 @@ METRIC = "fused draft+verify attn: query-tokens/s and KV HBM GB/s vs GB300 peak"
 UNIT = "query-tokens/s"
 
 
-def _traffic_ratio():
-    """DRAM traffic / algorithmic bytes of the attention kernel from the committed ncu
-    summary, if it was taken on the current source; else None."""
+def source_sha() -> str:
+    """Prefix of the sha256 of the fused kernel's sources (attn.cu, then topk.cuh)."""
     import hashlib
+    h = hashlib.sha256()
+    for f in ("attn.cu", "topk.cuh"):
+        with open(os.path.join(ROOT, "sparse_self_speculative_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_ratio(with_selection: bool):
+    """DRAM traffic / algorithmic bytes of the fused launch (with or without the
+    selection inside it) from the committed ncu summary, if that was taken on the
+    current sources; else None."""
     prof = os.path.join(ROOT, "profiles", "attn_persistent_qwen3_1p7b_b48.md")
-    src = os.path.join(ROOT, "sparse_self_speculative_gb300", "csrc", "attn.cu")
+    key = "traffic_ratio_with_selection:" if with_selection else "traffic_ratio:"
     try:
         text = open(prof).read()
-        ratio = float(text.split("traffic_ratio:")[1].split()[0])
-        sha = text.split("attn_cu_sha256_prefix:")[1].split()[0]
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != sha:
+        ratio = float(text.split(key)[1].split()[0])
+        if text.split("source_sha256_prefix:")[1].split()[0] != source_sha():
             return None
         return ratio
     except Exception:
@@ -232,10 +241,15 @@ def run_ours(args, world, rank, local):
     st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="setup")
     acc = step_accounting(st)
     stream = torch.cuda.current_stream()
+    S = st.score_buffer()
+    fused_sel = args.select == "fused"
 
     def step():
-        st.fused()
-        st.select()
+        if fused_sel:
+            st.fused_select(S)          # one launch: attention, then selection of the verified heads
+        else:
+            st.fused()
+            st.select(avg_scores=S)
 
     clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
@@ -254,15 +268,20 @@ def run_ours(args, world, rank, local):
     start.record(stream)
     for i in range(args.steps):
         ev_f0[i].record(stream)
-        st.fused()
-        ev_f1[i].record(stream)
-        st.select()
+        if fused_sel:
+            st.fused_select(S)
+            ev_f1[i].record(stream)
+        else:
+            st.fused()
+            ev_f1[i].record(stream)
+            st.select(avg_scores=S)
         ev_s1[i].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
     clk_hi = clk.mark()
     clk.__exit__()
     barrier(world)
+    assert hz.device_error(st.ws) == 0, "device error word set"
     total_ms = start.elapsed_time(stop)
     fused_ms = [a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)]
     select_ms = [a.elapsed_time(b) for a, b in zip(ev_f1, ev_s1)]
@@ -304,13 +323,46 @@ def run_ours(args, world, rank, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     e2e_value = tokens_all / (e2e_ms * args.steps / 1e3)
 
+    # context: the other selection layout, timed briefly on the same inputs
+    other = "separate" if fused_sel else "fused"
+
+    def other_step():
+        if fused_sel:
+            st.fused()
+            st.select(avg_scores=S)
+        else:
+            st.fused_select(S)
+    for _ in range(3):
+        other_step()
+    torch.cuda.synchronize()
+    o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_other = min(args.steps, 50)
+    o0.record(stream)
+    for _ in range(n_other):
+        other_step()
+    o1.record(stream)
+    torch.cuda.synchronize()
+    other_ms = o0.elapsed_time(o1) / n_other
+    # context: the attention launch alone (no selection), for its own roofline
+    for _ in range(3):
+        st.fused()
+    torch.cuda.synchronize()
+    o0.record(stream)
+    for _ in range(n_other):
+        st.fused()
+    o1.record(stream)
+    torch.cuda.synchronize()
+    attn_only_ms = o0.elapsed_time(o1) / n_other
+
     peak, peak_kind = _peaks()
     f_ms = statistics.mean(fused_ms)
-    achieved = acc["fused_bytes"] / (f_ms / 1e3) / 1e9
-    ratio = _traffic_ratio()
-    traffic = None if ratio is None else acc["fused_bytes"] * ratio
+    # the dominant kernel: the fused launch (with the selection when it runs inside it)
+    kbytes = acc["fused_bytes"] + (acc["select_bytes"] if fused_sel else 0)
+    achieved = kbytes / (f_ms / 1e3) / 1e9
+    ratio = _traffic_ratio(fused_sel)
+    traffic = None if ratio is None else kbytes * ratio
     kv_gbs = acc["kv_bytes"] / (f_ms / 1e3) / 1e9
-    gpu_launches = 2 * args.steps
+    gpu_launches = (1 if fused_sel else 2) * args.steps
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -321,10 +373,19 @@ def run_ours(args, world, rank, local):
                    "l2": f"inputs larger than L2 ({(acc['fused_bytes'] + acc['select_bytes']) / 1e9:.2f} GB read "
                          f"or written per step vs 129 MB of L2; no flush)"},
         "kv_gbs": kv_gbs,
-        "fused_ms": f_ms, "select_ms": statistics.mean(select_ms),
+        "selection": "inside the fused launch" if fused_sel else "separate launch",
+        "fused_ms": f_ms, "select_ms": None if fused_sel else statistics.mean(select_ms),
+        f"ms_per_step_{other}_selection": other_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "attn_persistent (fused step)", "peak_kind": peak_kind,
+                     "traffic": traffic,
+                     "kernel": "attn_persistent (fused step" + (" with selection)" if fused_sel else ")"),
+                     "algorithmic_bytes": kbytes, "peak_kind": peak_kind,
                      "kv_gbs": kv_gbs, "kv_frac": kv_gbs / peak},
+        "roofline_attention_only": {
+            "kernel": "attn_persistent (fused step without selection)", "ms": attn_only_ms,
+            "achieved": acc["fused_bytes"] / (attn_only_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": acc["fused_bytes"] / (attn_only_ms / 1e3) / 1e9 / peak,
+            "traffic": None if _traffic_ratio(False) is None else acc["fused_bytes"] * _traffic_ratio(False)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(clk_lo, clk_hi),
@@ -568,6 +629,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="first N requests of the workload (profiling cases)")
+    ap.add_argument("--select", default="fused", choices=["fused", "separate"],
+                    help="pillar selection inside the fused launch, or as its own launch after it")
     ap.add_argument("--sweep", action="store_true", help="context x batch x sparsity x stride sweep (JSON lines)")
     ap.add_argument("--sweep-L", default="1024,4096,16384,65536,131072")
     ap.add_argument("--sweep-B", default="1,16,64,256")

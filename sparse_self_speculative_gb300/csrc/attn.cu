@@ -275,11 +275,11 @@ __device__ int next_task(const AttnParams& p, long long total, uint32_t total_av
 // Publishes the averaging items of (r, h) once its output and LSE are written (all
 // threads call it).
 template <int NT>
-__device__ void publish_avg(const AttnParams& p, int r, int h, int L) {
+__device__ void publish_avg(const AttnParams& p, int r, int h, int L, int passes) {
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int blk = NT * kAvgPerThread;
+    const int blk = NT * kAvgPass * passes;
     const int nb = (L + blk - 1) / blk;
     const uint32_t base = atomicAdd(p.avg_reserve, uint32_t(nb));
     for (int b = 0; b < nb; ++b)
@@ -287,13 +287,13 @@ __device__ void publish_avg(const AttnParams& p, int r, int h, int L) {
   }
 }
 
-// One averaging item (queue slot `slot`): averages NT * kAvgPerThread positions of one
+// One averaging item (queue slot `slot`): averages NT * kAvgPass * passes positions of one
 // verifying (request, kv head) from the logit dump and LSE, adds their first radix digit
 // to the head's histogram; the head's last item runs its Top-K.  `ring` is the CTA's
 // K/V staging ring (64 KB, idle between units).
 template <int NT>
-__device__ void avg_item(const AttnParams& p, uint32_t slot, uint8_t* ring, int* s_misc, int* s_warp) {
-  constexpr int kBlk = NT * kAvgPerThread;
+__device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t* ring, int* s_misc, int* s_warp) {
+  const int kBlk = NT * kAvgPass * passes;
   constexpr int kCand = 6144;
   constexpr int kAvgRowGroup = 8;   // 64 loads in flight a thread: the attention kernel has the registers
   static_assert(SSPEC_MAX_ROWS % kAvgRowGroup == 0, "row groups fit s_lse");
@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   // (rebuilt once when it reaches the draft units); the first build also counts the
   // draft units and the averaging items of the fused selection ----
   uint32_t total_avg = 0;
+  int avg_passes = 1;
   long long n_draft = 0;
   auto build_prefix = [&](bool verify_phase, bool first) -> long long {
     const int per = (B + kThreads - 1) / kThreads;
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
           if (q.verify == verify_phase) units = n; else other += n;
           int K;
           if (first && p.sel_scores != nullptr && q.verify && sel_request_ok(p, r, q, &K, blockIdx.x == 0))
-            avg_sum += ((q.L + kThreads * kAvgPerThread - 1) / (kThreads * kAvgPerThread)) * p.hkv;
+            avg_sum += ((q.L + kThreads * kAvgPass - 1) / (kThreads * kAvgPass)) * p.hkv;
         }
         s_prefix[r + 1] = units;
       }
@@ -414,10 +415,24 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     }
     if (first) {
       int t;
-      block_exclusive_scan<kThreads>(avg_sum, s_warp, &t);
-      total_avg = uint32_t(t);
       block_exclusive_scan<kThreads>(other, s_warp, &t);
       n_draft = t;
+      // averaging items of one pass each, then the passes per item for about one item a CTA
+      block_exclusive_scan<kThreads>(avg_sum, s_warp, &t);
+      avg_passes = min(kAvgMaxPasses, max(1, t / int(gridDim.x)));
+      if (t > 0) {
+        const int blk = kThreads * kAvgPass * avg_passes;
+        avg_sum = 0;
+        for (int i = 0; i < per; ++i) {
+          const int r = tid * per + i;
+          Req q;
+          int K;
+          if (r < B && load_req(p, r, q, false) && q.verify && sel_request_ok(p, r, q, &K, false))
+            avg_sum += ((q.L + blk - 1) / blk) * p.hkv;
+        }
+        block_exclusive_scan<kThreads>(avg_sum, s_warp, &t);
+      }
+      total_avg = uint32_t(t);
     }
     int total;
     int run = block_exclusive_scan<kThreads>(sum, s_warp, &total);
@@ -455,7 +470,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     const int kind = s_misc[3];
     if (kind == 0) break;
     if (kind == 2) {
-      avg_item<kThreads>(p, uint32_t(s_misc[0]), smem + S::off_k, s_misc, s_warp);
+      avg_item<kThreads>(p, uint32_t(s_misc[0]), avg_passes, smem + S::off_k, s_misc, s_warp);
       continue;
     }
     const long long u = s_misc[0];   // unit index over both phases (names its partial state)
@@ -786,7 +801,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       }
       if (total_avg > 0 && q.verify) {
         int K;
-        if (sel_request_ok(p, r, q, &K, false)) publish_avg<kThreads>(p, r, h, q.L);
+        if (sel_request_ok(p, r, q, &K, false)) publish_avg<kThreads>(p, r, h, q.L, avg_passes);
       }
     } else {
       const size_t ustride = size_t(p.unit_stride);
@@ -818,7 +833,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
         if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
         if (total_avg > 0 && q.verify) {
           int K;
-          if (sel_request_ok(p, r, q, &K, false)) publish_avg<kThreads>(p, r, h, q.L);
+          if (sel_request_ok(p, r, q, &K, false)) publish_avg<kThreads>(p, r, h, q.L, avg_passes);
         }
       }
     }

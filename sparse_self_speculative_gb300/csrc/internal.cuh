@@ -32,12 +32,12 @@ constexpr int kSelBins = 1 << kSelBits1;
 constexpr int kSelSegment = 16384; // positions per compaction segment
 
 // ---- selection inside the fused step ---------------------------------------------------
-// An averaging item covers kAvgPerThread positions per attention thread (4096 to 8192
-// positions), averaged kAvgPass per thread at a time; a (request, kv head) has at most
-// kMaxAvgItems of them.
+// An averaging item covers 1 to kAvgMaxPasses passes of kAvgPass positions per attention
+// thread (the count is chosen per launch so that there are about as many items as
+// CTAs); a (request, kv head) has at most kMaxAvgItems of them.
 constexpr int kAvgPass = 8;
-constexpr int kAvgPerThread = 4 * kAvgPass;
-constexpr int kMaxAvgItems = (kMaxChunks * kChunk + 4095) / 4096;
+constexpr int kAvgMaxPasses = 4;
+constexpr int kMaxAvgItems = (kMaxChunks * kChunk + 1023) / 1024;
 
 // ---- workspace layout ------------------------------------------------------------------
 // [0, 512)        header: error word and the persistent-kernel queue counters (the
