@@ -110,3 +110,29 @@ def test_host_validation_rejects_before_launch(lib):
     rc = lib.sspec_sparse_draft_attn(ctypes.byref(shape), ctypes.byref(kv), 1, 16, 16, 16, None, 16, 16, 16, 16,
                                      256, 1 << 20, None)
     assert rc == ss.SSPEC_ERR_INVALID_ARG
+
+
+def test_fused_step_select_host_validation(lib):
+    """The single-launch step with selection rejects a bad sparsity, a missing
+    averages buffer, dump or pillar arrays, and a bad verify bucket before launching."""
+    shape = ss.make_shape(16, 8)
+    kv = ss.SspecPagedKV(4096, 4096, 4096, 4, 10)
+    fn = lib.sspec_fused_step_select
+    fn.restype = ctypes.c_int
+    P = ctypes.c_void_p
+
+    def call(s=0.05, verify_bucket=0, avg=16, logits=16, loff=16, idx=16, nsel=16, batch=1):
+        return fn(ctypes.byref(shape), ctypes.byref(kv), ctypes.c_int32(batch), ctypes.c_int32(8), P(16),
+                  ctypes.c_int32(verify_bucket), P(16), P(16), P(16), P(16), P(idx), P(16), P(nsel),
+                  ctypes.c_float(s), P(avg), P(16), P(16), P(logits), P(loff), P(256), ctypes.c_size_t(1 << 20),
+                  None)
+
+    for s in (0.0, -0.5, 1.01, float("nan")):
+        assert call(s=s) == ss.SSPEC_ERR_INVALID_ARG
+    assert call(avg=None) == ss.SSPEC_ERR_INVALID_ARG
+    assert call(logits=None) == ss.SSPEC_ERR_INVALID_ARG
+    assert call(loff=None) == ss.SSPEC_ERR_INVALID_ARG
+    assert call(idx=None) == ss.SSPEC_ERR_INVALID_ARG
+    assert call(nsel=None) == ss.SSPEC_ERR_INVALID_ARG
+    assert call(verify_bucket=9) == ss.SSPEC_ERR_INVALID_ARG
+    assert call(batch=0) == ss.SSPEC_OK                       # nothing to do, nothing launched
