@@ -290,36 +290,67 @@ def run_ours(args, world, rank, local):
     value = tokens_all / (ms_step * args.steps / 1e3)
 
     # ---- end to end: host buffers in, results out, every step ----
+    # As a serving loop runs it: two sets of per-step device buffers, host-to-device
+    # and device-to-host copies each on a stream of their own, so that step t+1's inputs
+    # go in and step t-1's results come out while step t's kernel runs.  The KV cache, workspace, dump and averages
+    # stay resident and are used by one kernel at a time (compute stream).
+    import copy as _copy
     pin = lambda t: t.cpu().pin_memory()
-    h_q, h_qoff = pin(st.d_q), pin(st.d_q_off)
-    h_seq, h_sel, h_bucket, h_nsel = pin(st.d_seq), pin(st.d_sel), pin(st.d_bucket), pin(st.d_nsel)
-    h_out = torch.empty_like(st.d_out, device="cpu").pin_memory()
-    h_lse = torch.empty_like(st.d_lse, device="cpu").pin_memory()
-    h_idx = torch.empty_like(st.d_idx, device="cpu").pin_memory()
-    ins = [(st.d_q, h_q), (st.d_q_off, h_qoff), (st.d_seq, h_seq), (st.d_sel, h_sel), (st.d_bucket, h_bucket),
-           (st.d_nsel, h_nsel)]
-    outs = [(h_out, st.d_out), (h_lse, st.d_lse), (h_idx, st.d_idx)]
-    h2d = sum(h.numel() * h.element_size() for _, h in ins)
-    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+    in_names = ["d_q", "d_q_off", "d_seq", "d_sel", "d_bucket", "d_nsel"]
+    out_names = ["d_out", "d_lse", "d_idx"]
+    h_in = {n: pin(getattr(st, n)) for n in in_names}
+    h_out = {n: torch.empty_like(getattr(st, n), device="cpu").pin_memory() for n in out_names}
+    h2d = sum(h.numel() * h.element_size() for h in h_in.values())
+    d2h = sum(h.numel() * h.element_size() for h in h_out.values())
+    sets = [st, _copy.copy(st)]
+    for n in in_names + out_names:
+        setattr(sets[1], n, getattr(st, n).clone())
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
 
-    def e2e_step():
-        for d, h in ins:
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in outs:
-            h.copy_(d, non_blocking=True)
+    def run_set(x):
+        if fused_sel:
+            x.fused_select(S)
+        else:
+            x.fused()
+            x.select(avg_scores=S)
 
-    for _ in range(2):
-        e2e_step()
+    def e2e_step(t):
+        b = t % 2
+        x = sets[b]
+        with torch.cuda.stream(h2d_stream):
+            h2d_stream.wait_event(ev["comp"][b])       # the set's previous kernel is done with its inputs
+            for n in in_names:
+                getattr(x, n).copy_(h_in[n], non_blocking=True)
+            ev["h2d"][b].record(h2d_stream)
+        stream.wait_event(ev["h2d"][b])
+        stream.wait_event(ev["d2h"][b])                 # its previous results have been read out
+        run_set(x)
+        ev["comp"][b].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(ev["comp"][b])
+            for n in out_names:
+                h_out[n].copy_(getattr(x, n), non_blocking=True)
+            ev["d2h"][b].record(d2h_stream)
+
+    for b in range(2):
+        for k in ev:
+            ev[k][b].record(stream)
+    for t in range(4):
+        e2e_step(t)
     torch.cuda.synchronize()
     barrier(world)
-    t0 = time.perf_counter()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    h2d_stream.wait_event(e0)
+    d2h_stream.wait_event(e0)
+    for t in range(args.steps):
+        e2e_step(t)
+    for b in range(2):
+        stream.wait_event(ev["d2h"][b])                 # the last results are on the host
     e1.record(stream)
     torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0, "device error word set"
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     e2e_value = tokens_all / (e2e_ms * args.steps / 1e3)
 
@@ -386,7 +417,9 @@ def run_ours(args, world, rank, local):
             "achieved": acc["fused_bytes"] / (attn_only_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
             "frac": acc["fused_bytes"] / (attn_only_ms / 1e3) / 1e9 / peak,
             "traffic": None if _traffic_ratio(False) is None else acc["fused_bytes"] * _traffic_ratio(False)},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "pinned host buffers, one stream per direction, two device buffer sets: step "
+                          "t+1 in and step t-1 out while step t's kernel runs"},
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(clk_lo, clk_hi),
         "bytes_per_step": {"kv": acc["kv_bytes"], "fused_total": acc["fused_bytes"], "select": acc["select_bytes"]},
