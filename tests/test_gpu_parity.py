@@ -360,14 +360,23 @@ def test_device_generator_matches_host():
         np.testing.assert_array_equal(hz.to_bits(t), host)
 
 
-@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (40, 8)])
-def test_fused_select_equals_separate_launches_bitwise(hq, hkv):
+@pytest.mark.parametrize("hq,hkv,s,long_lens", [
+    (16, 8, 0.05, [9000]),
+    (32, 8, 0.05, [9000]),
+    (40, 8, 0.05, [9000]),
+    # K = 8,000 and 12,000 exceed the fused path's candidate list: its multi-pass Top-K
+    (16, 8, 0.4, [20000, 30000]),
+])
+def test_fused_select_equals_separate_launches_bitwise(hq, hkv, s, long_lens):
     """Selection inside the fused launch writes exactly what the fused step followed by
     the standalone selection writes: outputs, LSE, dump, averages, pillars and counts;
     a second call (queue counters and slots reset by the first) gives the same again."""
-    k, s = 8, 0.05
+    k = 8
     rng = np.random.default_rng(hq + 1000)
-    lens = np.concatenate([[9000, 64, 1025, 3072, 1536, 2049], rng.integers(40, 5000, size=30)]).astype(np.int32)
+    lens = np.concatenate([[long_lens[0], 64, 1025, 3072, 1536, 2049], rng.integers(40, 5000, size=30)])
+    for i, L in enumerate(long_lens[1:]):
+        lens[9 * (i + 1)] = L          # requests 0, 9, 18, ... verify (bucket 0)
+    lens = lens.astype(np.int32)
     wl = synth.make_workload("fsel", 4242 + hq, hq, hkv, lens, plant="kv_per_head", plant_frac=0.01)
     import sparse_self_speculative_gb300 as ss
     buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), len(lens))
