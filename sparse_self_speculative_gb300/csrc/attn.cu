@@ -8,11 +8,11 @@
 // "Unified batch scheduler", paper Sec. 4.2 / Fig. 15) serving PillarAttn
 // (section "PillarAttn", paper Sec. 4.1).
 //
-// Work decomposition: a unit is (request, kv head, chunk of kChunk entries of
-// the request's token list).  Verification lists positions 0..L-1, a draft
-// step its pillars then its tail.  Units are handed out by an atomic counter
-// (no CTA ever waits on another); each unit writes a partial softmax state
-// and the last unit of a (request, head) to arrive merges them.
+// Work decomposition: a unit is (request, kv head, chunk of the request's
+// token list: 768, 1536 or 3072 positions to verify, 768 entries of a draft step).
+// Verification lists positions 0..L-1, a draft step its pillars then its tail.
+// Units are handed out by an atomic counter; each unit writes a partial softmax
+// state and the last unit of a (request, head) to arrive merges them.
 //
 // Inside a unit, K/V rows (256 B per token and head) are staged with 16-byte
 // cp.async into an XOR-swizzled shared-memory ring, and both products run on
@@ -394,6 +394,33 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   uint32_t total_avg = 0;
   int avg_passes = 1;
   long long n_draft = 0;
+  // ---- the verification chunk of this launch: the longest of 4, 2 or 1 times kChunk
+  // that still gives every CTA about 1.5 units (long units cost fewer unit starts and
+  // merges; small batches need the parallelism) ----
+  int vchunk = kChunk;
+  {
+    const int per = (B + kThreads - 1) / kThreads;
+    int u4 = 0, u2 = 0, ud = 0;
+    for (int i = 0; i < per; ++i) {
+      const int r = tid * per + i;
+      Req q;
+      if (r < B && load_req(p, r, q, false)) {
+        if (q.verify) {
+          u4 += ((q.T + 4 * kChunk - 1) / (4 * kChunk)) * p.hkv;
+          u2 += ((q.T + 2 * kChunk - 1) / (2 * kChunk)) * p.hkv;
+        } else {
+          ud += ((q.T + kChunk - 1) / kChunk) * p.hkv;
+        }
+      }
+    }
+    int t4, t2, td;
+    block_exclusive_scan<kThreads>(u4, s_warp, &t4);
+    block_exclusive_scan<kThreads>(u2, s_warp, &t2);
+    block_exclusive_scan<kThreads>(ud, s_warp, &td);
+    const int want = 3 * int(gridDim.x) / 2;
+    vchunk = t4 + td >= want ? 4 * kChunk : (t2 + td >= want ? 2 * kChunk : kChunk);
+  }
+
   auto build_prefix = [&](bool verify_phase, bool first) -> long long {
     const int per = (B + kThreads - 1) / kThreads;
     int sum = 0, other = 0, avg_sum = 0;
@@ -403,7 +430,8 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       if (r < B) {
         Req q;
         if (load_req(p, r, q, first && blockIdx.x == 0)) {
-          const int n = ((q.T + kChunk - 1) / kChunk) * p.hkv;
+          const int chunk = q.verify ? vchunk : kChunk;
+          const int n = ((q.T + chunk - 1) / chunk) * p.hkv;
           if (q.verify == verify_phase) units = n; else other += n;
           int K;
           if (first && p.sel_scores != nullptr && q.verify && sel_request_ok(p, r, q, &K, blockIdx.x == 0))
@@ -495,14 +523,18 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     const int nch = (s_prefix[r + 1] - s_prefix[r]) / p.hkv;
     const int local = int(ul - s_prefix[r]);
     const int h = local / nch, c = local % nch;
-    const int tok0 = c * kChunk;
-    const int ntok = min(q.T - tok0, kChunk);
+    const int chunk = q.verify ? vchunk : kChunk;
+    const int tok0 = c * chunk;
+    const int ntok = min(q.T - tok0, chunk);
     const int mt_used = (q.rows + 15) >> 4;
     const int G = p.group;
 
-    // ---- 1. row ids (page * Hkv + h) * 16 + slot of every entry of the chunk ----
-    for (int i = tid; i < ntok; i += kThreads) {
-      const int e = tok0 + i;
+    // ---- 1. row ids (page * Hkv + h) * 16 + slot: one per 16-token page of a
+    // verification chunk (its positions are contiguous and start on a page), one per
+    // entry of a draft chunk ----
+    const int nids = q.verify ? (ntok + kPage - 1) / kPage : ntok;
+    for (int i = tid; i < nids; i += kThreads) {
+      const int e = q.verify ? tok0 + i * kPage : tok0 + i;
       int pos;
       int bad = 0;
       if (q.verify) {
@@ -525,6 +557,13 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       }
       s_row[i] = rid;
     }
+
+    // row id of entry i of the chunk (-1: not loadable)
+    auto row_id = [&](int i) -> int {
+      if (!q.verify) return s_row[i];
+      const int b = s_row[i >> 4];
+      return b < 0 ? -1 : b + (i & (kPage - 1));
+    };
 
     // ---- 2. query rows of this kv head into shared memory (zero padded) ----
     for (int e = tid; e < MT * 16 * 16; e += kThreads) {
@@ -554,7 +593,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
         if ((kTile * 16) % kThreads != 0 && e >= kTile * 16) break;
         const int row = e >> 4, ch = e & 15;
         const int i = t * kTile + row;
-        const int rid = (i < ntok) ? s_row[i] : -1;
+        const int rid = (i < ntok) ? row_id(i) : -1;
         const size_t off = size_t(rid < 0 ? 0 : rid) * kHeadDim + ch * 8;
         cp_async16(kb + swz256(row, ch), p.k_cache + off, rid >= 0);
         cp_async16(vb + swz256(row, ch), p.v_cache + off, rid >= 0);
@@ -649,7 +688,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
 #pragma unroll
             for (int ii = 0; ii < 2; ++ii) {
               const int i = t * kTile + ng * 8 * NT + nt * 8 + tq * 2 + ii;
-              const bool valid = i < ntok && s_row[i] >= 0;
+              const bool valid = i < ntok && row_id(i) >= 0;
               const int pos = tok0 + i;
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {

@@ -14,15 +14,16 @@ constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
 
 // ---- attention work decomposition -------------------------------------------------
-// A work unit is (request, kv head, chunk of kChunk tokens of that request's token
-// list).  Verification lists positions 0..L-1; a draft step lists its pillars then
-// its tail.  Chunks are merged through their (o, m, l) partial states.
-constexpr int kChunk = 768;
+// A work unit is (request, kv head, chunk of that request's token list: 1, 2 or 4
+// times kChunk positions to verify (chosen per launch), kChunk entries of a draft step).  Verification lists positions
+// 0..L-1; a draft step lists its pillars then its tail.  Chunks are merged through
+// their (o, m, l) partial states.
+constexpr int kChunk = 768;        // entries of a draft unit (row ids held per entry)
+constexpr int kVerifyChunkMax = 4 * kChunk;   // longest verification unit (row ids per 16-token page)
 constexpr int kMaxChunks = 256;    // per (request, kv head): bounds the merge scratch
 constexpr int kTile = 64;          // tokens per pipeline stage
 constexpr int kStages = 2;         // cp.async pipeline depth (two CTAs per SM for every shape)
-constexpr int kAttnWarps = 4;      // warps per CTA when the query rows fit one 16-row MMA tile
-constexpr int kAttnWarpsWide = 8;  // warps per CTA for 2-4 row tiles (verification with k*G > 16)
+static_assert(kChunk % kTile == 0 && kVerifyChunkMax / kPage <= kChunk, "verification unit row ids fit");
 
 // ---- selection work decomposition ----------------------------------------------------
 constexpr int kSelBlock = 4096;    // tokens averaged per unit

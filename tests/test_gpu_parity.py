@@ -164,12 +164,15 @@ def test_sparse_draft_parity(hq, hkv, lens, steps):
         assert np.abs(lb[r] - l_ref).max() <= LSE_TOL
 
 
-def test_sparse_with_every_token_equals_full_verify_bitwise():
+def test_sparse_with_every_token_equals_full_verify():
     """s = 1: the pillar set is every position, so the draft step attends to the
-    same ordered token list as one-query verification and must give the same bits."""
+    same ordered token list as one-query verification.  Requests that fit one draft
+    unit (768 entries) give the same bits; longer ones may be split differently
+    (768-entry draft units; verification units of up to 3072 tokens, chosen per
+    launch) and agree to rounding."""
     import sparse_self_speculative_gb300 as ss
     hq, hkv = 16, 8
-    lens = [1500, 513, 64]
+    lens = [1500, 513, 64, 4000]
     wl = synth.make_workload("s1", 9, hq, hkv, lens)
     B = wl.batch
     dkv = hz.DeviceKV(wl, fill="host")
@@ -192,8 +195,15 @@ def test_sparse_with_every_token_equals_full_verify_bitwise():
                          out_v, lse_v, None, None, ws)
     torch.cuda.synchronize()
     assert hz.device_error(ws) == 0
-    np.testing.assert_array_equal(hz.to_bits(out_s), hz.to_bits(out_v)[:, 0])
-    np.testing.assert_array_equal(lse_s.cpu().numpy(), lse_v.cpu().numpy()[:, 0])
+    os_, ov = hz.to_bits(out_s), hz.to_bits(out_v)[:, 0]
+    ls, lv = lse_s.cpu().numpy(), lse_v.cpu().numpy()[:, 0]
+    for r in range(B):
+        if L[r] <= 768:          # one unit each: identical arithmetic
+            np.testing.assert_array_equal(os_[r], ov[r])
+            np.testing.assert_array_equal(ls[r], lv[r])
+        else:
+            hz.check_close_bf16(os_[r], oracle.bf16_bits_to_f64(ov[r]), 4e-3, 8e-3)
+            assert np.abs(ls[r] - lv[r]).max() <= 1e-5
 
 
 def _select_check(st, r, S_dev):
