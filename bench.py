@@ -334,8 +334,8 @@ def run_ours(args, world, rank, local):
             ev["d2h"][b].record(d2h_stream)
 
     for b in range(2):
-        for k in ev:
-            ev[k][b].record(stream)
+        for kind in ev:
+            ev[kind][b].record(stream)
     for t in range(4):
         e2e_step(t)
     torch.cuda.synchronize()
