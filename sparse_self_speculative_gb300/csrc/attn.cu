@@ -386,81 +386,97 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   const int g8 = lane >> 2, tq = lane & 3;
   const int B = p.batch;
 
-  // ---- the attention queue holds every verification unit first, then every draft
-  // unit: long units start early, and the selection of verified heads overlaps the
-  // drafts.  s_prefix holds the per-request unit prefix of the phase the CTA is in
-  // (rebuilt once when it reaches the draft units); the first build also counts the
-  // draft units and the averaging items of the fused selection ----
+  // The attention queue holds every verification unit first, then every draft unit:
+  // long units start early, and the selection of verified heads overlaps the drafts.
+  // s_prefix holds the per-request unit prefix of the phase the CTA is in (rebuilt
+  // once when it reaches the draft units).
+  //
+  // ---- start-up: each thread reads its requests' descriptions once (kept in
+  // registers until the prefix is built).  The verification chunk of this launch is
+  // the longest of 4, 2 or 1 times kChunk that still gives every CTA about 1.5 units
+  // (long units cost fewer unit starts and merges; small batches need the
+  // parallelism); the averaging items of the fused selection get 1 to 4 passes, for
+  // about one item per CTA. ----
+  constexpr int kPer = (SSPEC_MAX_BATCH + kThreads - 1) / kThreads;
+  const int per = (B + kThreads - 1) / kThreads;
+  int rT[kPer], rL[kPer], rflags[kPer];   // flags: 1 valid, 2 verifies, 4 takes part in the selection
+  int vchunk = kChunk, avg_passes = 1;
   uint32_t total_avg = 0;
-  int avg_passes = 1;
   long long n_draft = 0;
-  // ---- the verification chunk of this launch: the longest of 4, 2 or 1 times kChunk
-  // that still gives every CTA about 1.5 units (long units cost fewer unit starts and
-  // merges; small batches need the parallelism) ----
-  int vchunk = kChunk;
   {
-    const int per = (B + kThreads - 1) / kThreads;
-    int u4 = 0, u2 = 0, ud = 0;
-    for (int i = 0; i < per; ++i) {
+    int u4 = 0, u2 = 0, u1 = 0, ud = 0, a1 = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
       const int r = tid * per + i;
+      rT[i] = rL[i] = rflags[i] = 0;
       Req q;
-      if (r < B && load_req(p, r, q, false)) {
+      if (i < per && r < B && load_req(p, r, q, blockIdx.x == 0)) {
+        int K;
+        const bool sel = p.sel_scores != nullptr && q.verify && sel_request_ok(p, r, q, &K, blockIdx.x == 0);
+        rT[i] = q.T;
+        rL[i] = q.L;
+        rflags[i] = 1 | (q.verify ? 2 : 0) | (sel ? 4 : 0);
         if (q.verify) {
           u4 += ((q.T + 4 * kChunk - 1) / (4 * kChunk)) * p.hkv;
           u2 += ((q.T + 2 * kChunk - 1) / (2 * kChunk)) * p.hkv;
+          u1 += ((q.T + kChunk - 1) / kChunk) * p.hkv;
         } else {
           ud += ((q.T + kChunk - 1) / kChunk) * p.hkv;
         }
+        if (sel) a1 += ((q.L + kThreads * kAvgPass - 1) / (kThreads * kAvgPass)) * p.hkv;
       }
     }
-    int t4, t2, td;
+    int t4, t2, t1, td, ta;
     block_exclusive_scan<kThreads>(u4, s_warp, &t4);
     block_exclusive_scan<kThreads>(u2, s_warp, &t2);
+    block_exclusive_scan<kThreads>(u1, s_warp, &t1);
     block_exclusive_scan<kThreads>(ud, s_warp, &td);
+    block_exclusive_scan<kThreads>(a1, s_warp, &ta);
     const int want = 3 * int(gridDim.x) / 2;
     vchunk = t4 + td >= want ? 4 * kChunk : (t2 + td >= want ? 2 * kChunk : kChunk);
-  }
-
-  auto build_prefix = [&](bool verify_phase, bool first) -> long long {
-    const int per = (B + kThreads - 1) / kThreads;
-    int sum = 0, other = 0, avg_sum = 0;
+    n_draft = td;
+    avg_passes = min(kAvgMaxPasses, max(1, ta / int(gridDim.x)));
+    const int blk = kThreads * kAvgPass * avg_passes;
+    int sum = 0, an = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int r = tid * per + i;
+      if (i < per && r < B) {
+        const bool verify = (rflags[i] & 2) != 0;
+        const int units = verify ? ((rT[i] + vchunk - 1) / vchunk) * p.hkv : 0;
+        if (rflags[i] & 4) an += ((rL[i] + blk - 1) / blk) * p.hkv;
+        s_prefix[r + 1] = units;
+        sum += units;
+      }
+    }
+    int t;
+    block_exclusive_scan<kThreads>(an, s_warp, &t);
+    total_avg = ta > 0 ? uint32_t(t) : 0u;
+    int run = block_exclusive_scan<kThreads>(sum, s_warp, &t);
     for (int i = 0; i < per; ++i) {
       const int r = tid * per + i;
-      int units = 0;
+      if (r < B) {
+        run += s_prefix[r + 1];
+        s_prefix[r + 1] = run;
+      }
+    }
+    if (tid == 0) s_prefix[0] = 0;
+    __syncthreads();
+  }
+  const long long n_verify = s_prefix[B];
+
+  // the draft phase's prefix, rebuilt once per CTA when it reaches the draft units
+  auto build_draft_prefix = [&]() {
+    int sum = 0;
+    for (int i = 0; i < per; ++i) {
+      const int r = tid * per + i;
       if (r < B) {
         Req q;
-        if (load_req(p, r, q, first && blockIdx.x == 0)) {
-          const int chunk = q.verify ? vchunk : kChunk;
-          const int n = ((q.T + chunk - 1) / chunk) * p.hkv;
-          if (q.verify == verify_phase) units = n; else other += n;
-          int K;
-          if (first && p.sel_scores != nullptr && q.verify && sel_request_ok(p, r, q, &K, blockIdx.x == 0))
-            avg_sum += ((q.L + kThreads * kAvgPass - 1) / (kThreads * kAvgPass)) * p.hkv;
-        }
+        int units = 0;
+        if (load_req(p, r, q, false) && !q.verify) units = ((q.T + kChunk - 1) / kChunk) * p.hkv;
         s_prefix[r + 1] = units;
+        sum += units;
       }
-      sum += units;
-    }
-    if (first) {
-      int t;
-      block_exclusive_scan<kThreads>(other, s_warp, &t);
-      n_draft = t;
-      // averaging items of one pass each, then the passes per item for about one item a CTA
-      block_exclusive_scan<kThreads>(avg_sum, s_warp, &t);
-      avg_passes = min(kAvgMaxPasses, max(1, t / int(gridDim.x)));
-      if (t > 0) {
-        const int blk = kThreads * kAvgPass * avg_passes;
-        avg_sum = 0;
-        for (int i = 0; i < per; ++i) {
-          const int r = tid * per + i;
-          Req q;
-          int K;
-          if (r < B && load_req(p, r, q, false) && q.verify && sel_request_ok(p, r, q, &K, false))
-            avg_sum += ((q.L + blk - 1) / blk) * p.hkv;
-        }
-        block_exclusive_scan<kThreads>(avg_sum, s_warp, &t);
-      }
-      total_avg = uint32_t(t);
     }
     int total;
     int run = block_exclusive_scan<kThreads>(sum, s_warp, &total);
@@ -473,9 +489,8 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     }
     if (tid == 0) s_prefix[0] = 0;
     __syncthreads();
-    return total;
   };
-  const long long n_verify = build_prefix(true, true);
+
   bool draft_phase = false;
   long long total = n_verify + n_draft;
   if (total > p.unit_capacity) {
@@ -505,7 +520,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     long long ul = u;                // index within the phase
     if (u >= n_verify) {
       if (!draft_phase) {
-        build_prefix(false, false);
+        build_draft_prefix();
         draft_phase = true;
       }
       ul = u - n_verify;
