@@ -53,6 +53,7 @@ struct Ws {
   int32_t* sel_cnt;
   uint32_t* sel_hist;
   unsigned long long* avg_slots;
+  int32_t* draft_base;
   uint8_t* region;
   size_t region_bytes;
 };
@@ -68,6 +69,7 @@ int carve(void* workspace, size_t ws_bytes, int batch, int hkv, Ws& w) {
   w.sel_cnt = reinterpret_cast<int32_t*>(b + kWsHeaderBytes + ws_counter_bytes(batch, hkv));
   w.sel_hist = reinterpret_cast<uint32_t*>(b + kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv));
   w.avg_slots = reinterpret_cast<unsigned long long*>(b + ws_avg_slot_offset(batch, hkv));
+  w.draft_base = reinterpret_cast<int32_t*>(b + ws_draft_base_offset(batch, hkv));
   w.region = b + off;
   w.region_bytes = ws_bytes - off;
   return SSPEC_OK;
@@ -133,6 +135,7 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
   p.q_done = &w.hdr->attn_done;
   p.merge_cnt = w.attn_cnt;
   p.partials = reinterpret_cast<float*>(w.region);
+  p.draft_base = w.draft_base;
   p.rows_max = any_verify ? nq * G : G;
   if (p.rows_max < G) p.rows_max = G;
   p.unit_stride = (long long)unit_partial_floats(p.rows_max);

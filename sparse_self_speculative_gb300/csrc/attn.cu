@@ -402,9 +402,9 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   int rT[kPer], rL[kPer], rflags[kPer];   // flags: 1 valid, 2 verifies, 4 takes part in the selection
   int vchunk = kChunk, avg_passes = 1;
   uint32_t total_avg = 0;
-  long long n_draft = 0;
+  long long n_draft = 0, n_full = 0;
   {
-    int u4 = 0, u2 = 0, u1 = 0, ud = 0, a1 = 0;
+    int u4 = 0, u2 = 0, u1 = 0, ud = 0, uf = 0, a1 = 0;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int r = tid * per + i;
@@ -422,19 +422,32 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
           u1 += ((q.T + kChunk - 1) / kChunk) * p.hkv;
         } else {
           ud += ((q.T + kChunk - 1) / kChunk) * p.hkv;
+          uf += ((q.T + kChunk - 1) / kChunk - 1) * p.hkv;
         }
         if (sel) a1 += ((q.L + kThreads * kAvgPass - 1) / (kThreads * kAvgPass)) * p.hkv;
       }
     }
-    int t4, t2, t1, td, ta;
+    int t4, t2, t1, td, tf, ta;
     block_exclusive_scan<kThreads>(u4, s_warp, &t4);
     block_exclusive_scan<kThreads>(u2, s_warp, &t2);
     block_exclusive_scan<kThreads>(u1, s_warp, &t1);
-    block_exclusive_scan<kThreads>(ud, s_warp, &td);
+    // each request's draft units take consecutive partial-state slots after all the
+    // verification units', (head, chunk)-major: slot = n_verify + draft_base[r] + h nch + c
+    int dbase = block_exclusive_scan<kThreads>(ud, s_warp, &td);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int r = tid * per + i;
+      if (i < per && r < B) {
+        p.draft_base[r] = dbase;
+        if ((rflags[i] & 3) == 1) dbase += ((rT[i] + kChunk - 1) / kChunk) * p.hkv;
+      }
+    }
+    block_exclusive_scan<kThreads>(uf, s_warp, &tf);
     block_exclusive_scan<kThreads>(a1, s_warp, &ta);
     const int want = 3 * int(gridDim.x) / 2;
     vchunk = t4 + td >= want ? 4 * kChunk : (t2 + td >= want ? 2 * kChunk : kChunk);
     n_draft = td;
+    n_full = tf;
     avg_passes = min(kAvgMaxPasses, max(1, ta / int(gridDim.x)));
     const int blk = kThreads * kAvgPass * avg_passes;
     int sum = 0, an = 0;
@@ -465,15 +478,20 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   }
   const long long n_verify = s_prefix[B];
 
-  // the draft phase's prefix, rebuilt once per CTA when it reaches the draft units
-  auto build_draft_prefix = [&]() {
+  // The draft units run in two sub-phases, longest first so that the launch ends on
+  // short units: every full kChunk-entry chunk (s_prefix: per-request prefix of those
+  // units), then the last chunk of every (request, head), requests ordered by the
+  // tile count of their last chunk in four bands, longest band first (s_prefix[j]:
+  // the j-th request; each has hkv units).  Each CTA builds these once, on reaching
+  // the sub-phase.
+  auto build_full_prefix = [&]() {
     int sum = 0;
     for (int i = 0; i < per; ++i) {
       const int r = tid * per + i;
       if (r < B) {
         Req q;
         int units = 0;
-        if (load_req(p, r, q, false) && !q.verify) units = ((q.T + kChunk - 1) / kChunk) * p.hkv;
+        if (load_req(p, r, q, false) && !q.verify) units = ((q.T + kChunk - 1) / kChunk - 1) * p.hkv;
         s_prefix[r + 1] = units;
         sum += units;
       }
@@ -490,8 +508,44 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     if (tid == 0) s_prefix[0] = 0;
     __syncthreads();
   };
+  auto last_band = [&](int r) -> int {   // -1: not a valid draft request
+    Req q;
+    if (!load_req(p, r, q, false) || q.verify) return -1;
+    const int last = q.T - ((q.T + kChunk - 1) / kChunk - 1) * kChunk;
+    const int tiles = (last + kTile - 1) / kTile;
+    return tiles > 9 ? 0 : (tiles > 6 ? 1 : (tiles > 3 ? 2 : 3));
+  };
+  auto build_last_order = [&]() {
+    int cnt[4] = {0, 0, 0, 0};
+    for (int i = 0; i < per; ++i) {
+      const int r = tid * per + i;
+      if (r < B) {
+        const int bd = last_band(r);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) cnt[x] += bd == x;
+      }
+    }
+    int before[4], off[4], tot;
+    int o = 0;
+#pragma unroll
+    for (int bd = 0; bd < 4; ++bd) {
+      before[bd] = block_exclusive_scan<kThreads>(cnt[bd], s_warp, &tot);
+      off[bd] = o;
+      o += tot;
+    }
+    for (int i = 0; i < per; ++i) {
+      const int r = tid * per + i;
+      if (r < B) {
+        const int bd = last_band(r);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          if (bd == x) s_prefix[off[x] + before[x]++] = r;
+      }
+    }
+    __syncthreads();
+  };
 
-  bool draft_phase = false;
+  int phase = 0;   // 0 verification units, 1 full draft chunks, 2 last draft chunks
   long long total = n_verify + n_draft;
   if (total > p.unit_capacity) {
     if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, SSPEC_DEVERR_WORKSPACE);
@@ -516,28 +570,56 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       avg_item<kThreads>(p, uint32_t(s_misc[0]), avg_passes, smem + S::off_k, s_misc, s_warp);
       continue;
     }
-    const long long u = s_misc[0];   // unit index over both phases (names its partial state)
-    long long ul = u;                // index within the phase
-    if (u >= n_verify) {
-      if (!draft_phase) {
-        build_draft_prefix();
-        draft_phase = true;
-      }
-      ul = u - n_verify;
-    }
-
-    // ---- decode the unit ----
-    int lo = 0, hi = B;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_prefix[mid] <= ul) lo = mid; else hi = mid;
-    }
-    const int r = lo;
+    const long long u = s_misc[0];   // unit index over all phases
+    // ---- decode the unit: request r, head h, chunk c of nch, partial-state slot ----
+    int r, h, c, nch;
+    long long slot;
     Req q;
-    load_req(p, r, q, false);
-    const int nch = (s_prefix[r + 1] - s_prefix[r]) / p.hkv;
-    const int local = int(ul - s_prefix[r]);
-    const int h = local / nch, c = local % nch;
+    if (u < n_verify) {
+      int lo = 0, hi = B;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_prefix[mid] <= u) lo = mid; else hi = mid;
+      }
+      r = lo;
+      nch = (s_prefix[r + 1] - s_prefix[r]) / p.hkv;
+      const int local = int(u - s_prefix[r]);
+      h = local / nch;
+      c = local % nch;
+      slot = u;
+      load_req(p, r, q, false);
+    } else if (u < n_verify + n_full) {
+      if (phase < 1) {
+        build_full_prefix();
+        phase = 1;
+      }
+      const long long ul = u - n_verify;
+      int lo = 0, hi = B;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_prefix[mid] <= ul) lo = mid; else hi = mid;
+      }
+      r = lo;
+      const int nfull = (s_prefix[r + 1] - s_prefix[r]) / p.hkv;
+      const int local = int(ul - s_prefix[r]);
+      h = local / nfull;
+      c = local % nfull;
+      nch = nfull + 1;
+      load_req(p, r, q, false);
+      slot = n_verify + __ldcg(p.draft_base + r) + (long long)h * nch + c;
+    } else {
+      if (phase < 2) {
+        build_last_order();
+        phase = 2;
+      }
+      const long long ul = u - n_verify - n_full;
+      r = s_prefix[int(ul / p.hkv)];
+      h = int(ul % p.hkv);
+      load_req(p, r, q, false);
+      nch = (q.T + kChunk - 1) / kChunk;
+      c = nch - 1;
+      slot = n_verify + __ldcg(p.draft_base + r) + (long long)h * nch + c;
+    }
     const int chunk = q.verify ? vchunk : kChunk;
     const int tok0 = c * chunk;
     const int ntok = min(q.T - tok0, chunk);
@@ -859,7 +941,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       }
     } else {
       const size_t ustride = size_t(p.unit_stride);
-      float* part = p.partials + size_t(u) * ustride;
+      float* part = p.partials + size_t(slot) * ustride;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int row = mg * 16 + g8 + hh * 8;
@@ -883,7 +965,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       __syncthreads();
       if (s_misc[1]) {
         __threadfence();
-        merge_partials<MT, W>(p, q, h, u - c, nch, reinterpret_cast<float*>(smem + S::off_k));
+        merge_partials<MT, W>(p, q, h, slot - c, nch, reinterpret_cast<float*>(smem + S::off_k));
         if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
         if (total_avg > 0 && q.verify) {
           int K;

@@ -46,6 +46,8 @@ constexpr int kMaxAvgItems = (kMaxChunks * kChunk + 1023) / 1024;
 // [256, ...)      per (request, kv head) arrival counters: attention, then selection
 //                 per (request, kv head) histograms of the first radix digit (selection)
 //                 averaging-item queue slots of the fused step (8 bytes each)
+//                 per-request first partial-state slot of its draft units (rewritten by
+//                 every attention launch)
 // [region, end)   attention partial states, or the averaged scores of selection
 // Everything before the region must be zero before the first call; every launch
 // leaves it zero.
@@ -77,8 +79,11 @@ inline size_t ws_avg_slot_bytes(int batch, int hkv) {
 inline size_t ws_avg_slot_offset(int batch, int hkv) {
   return kWsHeaderBytes + 2 * ws_counter_bytes(batch, hkv) + ws_hist_bytes(batch, hkv);
 }
-inline size_t ws_region_offset(int batch, int hkv) {
+inline size_t ws_draft_base_offset(int batch, int hkv) {
   return ws_avg_slot_offset(batch, hkv) + ws_avg_slot_bytes(batch, hkv);
+}
+inline size_t ws_region_offset(int batch, int hkv) {
+  return ws_draft_base_offset(batch, hkv) + align_up(size_t(batch) * sizeof(int32_t), 256);
 }
 // one unit's partial state: O [rows][128] fp32, then m [rows], l [rows]; the stride
 // is padded to 4 floats so every O row starts 16-byte aligned
@@ -123,6 +128,7 @@ struct AttnParams {
   long long unit_capacity;
   int rows_max;               // rows of a partial state
   long long unit_stride;      // floats between consecutive partial states
+  int32_t* draft_base;        // [batch]: first partial-state slot of each request's draft units
   // pillar selection of the verifying requests inside the same launch (sel_scores null: off)
   float sel_s;
   float* sel_scores;          // averages of request r at logit_off[r] / (nq * group)
