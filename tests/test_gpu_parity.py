@@ -87,6 +87,54 @@ def test_verify_parity(hq, hkv, lens):
         assert np.all(np.abs(lg[~masked] - lg_ref[~masked]) <= 1e-4 + 1e-5 * np.abs(lg_ref[~masked]))
 
 
+@pytest.mark.parametrize("hq,hkv,nq,lens", [
+    (16, 8, 9, [9, 10, 700, 2100]),      # k + 1 = 9 verify queries (bonus token): 18 rows, two tiles
+    (40, 8, 9, [9, 300, 1500]),          # 45 rows: three tiles
+    (8, 1, 7, [7, 500]),                 # 56 rows: four tiles
+    (32, 8, 1, [1, 2, 40, 1000]),        # one query: plain decode attention with the dump
+    (16, 8, 3, [3, 64, 2500]),
+])
+def test_verify_and_select_with_nq_queries(hq, hkv, nq, lens):
+    """Verification and selection take the verify query count nq as a parameter,
+    so the bonus-token reading (k + 1 queries) and plain decode are calls with a
+    different nq; the average's divisor becomes nq * G."""
+    import sparse_self_speculative_gb300 as ss
+    s = 0.05
+    wl = synth.make_workload("nq", 300 + 10 * nq + hq, hq, hkv, lens, plant="kv_per_head", plant_frac=0.02)
+    dkv, q, loff, d, shape, ws = _verify_batch(wl, nq)
+    _run_verify(dkv, d, shape, ws, wl.batch, nq)
+    B, G = wl.batch, hq // hkv
+    L = wl.seq_lens.astype(np.int64)
+    K = np.array([oracle.pillar_count(s, int(x)) for x in L], dtype=np.int64)
+    idx_off = np.zeros(B + 1, dtype=np.int64)
+    idx_off[1:] = np.cumsum(hkv * K)
+    q_off = (np.arange(B + 1) * nq).astype(np.int64)
+    S = torch.empty(int(hkv * L.sum()), dtype=torch.float32, device="cuda")
+    idx = torch.full((int(idx_off[-1]),), -1, dtype=torch.int32, device="cuda")
+    nsel = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ss.sspec_select_pillars(shape, B, nq, s, d["logits"], d["loff"], d["lse"], torch.from_numpy(q_off).cuda(),
+                            d["seq"], S, idx, torch.from_numpy(idx_off).cuda(), nsel, ws)
+    torch.cuda.synchronize()
+    assert hz.device_error(ws) == 0
+    out, lse = hz.to_bits(d["out"]), d["lse"].cpu().numpy()
+    Sh, idxh = S.cpu().numpy().astype(np.float64), idx.cpu().numpy()
+    np.testing.assert_array_equal(nsel.cpu().numpy(), K)
+    soff = 0
+    for r in range(B):
+        Lr = int(L[r])
+        kf, vf = (oracle.bf16_bits_to_f64(wl.kv_rows(w, r, np.arange(Lr))) for w in "kv")
+        o_ref, l_ref, lg_ref = oracle.verify_attention(oracle.bf16_bits_to_f64(q[r]), kf, vf, hz.SCALE)
+        hz.check_close_bf16(out[r], o_ref, OUT_ATOL, OUT_RTOL)
+        assert np.abs(lse[r] - l_ref).max() <= LSE_TOL
+        S_ref = oracle.average_scores(lg_ref, l_ref, G)
+        Sg = Sh[soff: soff + hkv * Lr].reshape(hkv, Lr)
+        soff += hkv * Lr
+        assert np.all(np.abs(Sg - S_ref) <= 1e-4 * np.abs(S_ref) + 1e-9)
+        for h in range(hkv):
+            got = idxh[idx_off[r] + h * K[r]: idx_off[r] + (h + 1) * K[r]]
+            np.testing.assert_array_equal(got, oracle.top_k_pillars(Sg[h], int(K[r])))
+
+
 def test_verify_page_permutation_and_causal_bit_identity():
     nq, hq, hkv = 8, 16, 8
     lens = [700, 129]
