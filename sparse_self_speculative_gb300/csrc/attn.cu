@@ -296,6 +296,7 @@ __device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t
   const int kBlk = NT * kAvgPass * passes;
   constexpr int kCand = 6144;
   constexpr int kAvgRowGroup = 8;   // 64 loads in flight a thread: the attention kernel has the registers
+  constexpr int kAvgAhead = 1;      // passes prefetched into L2 ahead of the pass being loaded
   static_assert(SSPEC_MAX_ROWS % kAvgRowGroup == 0, "row groups fit s_lse");
   static_assert(kSelBins * 4 + SSPEC_MAX_ROWS * 4 + 2 * NT * 4 + 2 * kCand * 4 <= 2 * kStages * kTile * kRowBytes,
                 "selection shared memory fits the K/V ring");
@@ -324,15 +325,23 @@ __device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t
   sel_request_ok(p, r, q, &K, false);
   const int G = p.group, L = q.L, rows = q.rows;
   const int nb = (L + kBlk - 1) / kBlk;
+  const float* lg = p.logits + q.loff + size_t(h) * rows * L;
+  const int t_end = min(L, (b + 1) * kBlk);
+  constexpr int kStep = NT * kAvgPass;
+  // the registers hold one pass of loads; L2 prefetches keep the next passes in flight
+  for (int a = 0; a < kAvgAhead; ++a)
+    sel::prefetch_pass<NT>(lg, L, rows, b * kBlk + a * kStep, min(t_end, b * kBlk + (a + 1) * kStep));
   for (int i = tid; i < kSelBins; i += NT) s_hist[i] = 0u;
   if (tid < SSPEC_MAX_ROWS)
     s_lse[tid] = tid < rows ? __ldcg(p.lse + size_t(q.qbase + tid / G) * p.hq + h * G + tid % G) : 0.f;
   __syncthreads();
   float* S = p.sel_scores + q.loff / rows + size_t(h) * L;
-  const int t_end = min(L, (b + 1) * kBlk);
-  for (int t_lo = b * kBlk; t_lo < t_end; t_lo += NT * kAvgPass)
-    sel::average_block<NT, kAvgPass, kAvgRowGroup, false>(p.logits + q.loff + size_t(h) * rows * L, L, rows, s_lse, t_lo,
-                                            min(t_end, t_lo + NT * kAvgPass), S, s_hist);
+  for (int t_lo = b * kBlk; t_lo < t_end; t_lo += kStep) {
+    const int t_nx = t_lo + kAvgAhead * kStep;
+    if (t_nx < t_end) sel::prefetch_pass<NT>(lg, L, rows, t_nx, min(t_end, t_nx + kStep));
+    sel::average_block<NT, kAvgPass, kAvgRowGroup, false>(lg, L, rows, s_lse, t_lo, min(t_end, t_lo + kStep), S,
+                                                          s_hist);
+  }
   __syncthreads();
   uint32_t* ghist = p.sel_hist + (size_t(r) * p.hkv + h) * kSelBins;
   for (int i = tid; i < kSelBins; i += NT) {
@@ -351,7 +360,7 @@ __device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t
     const long long ibase = p.idx_off[r];
     const long long istride = (p.idx_off[r + 1] - ibase) / p.hkv;
     const sel::TopkSmem sm{s_hist, s_gt, s_eq, s_pos, s_key, s_misc, s_warp, kCand};
-    sel::topk_ascending<NT>(S, L, K, ghist, p.sel_idx + ibase + h * istride, sm);
+    sel::topk_ascending<NT, 32, true>(S, L, K, ghist, p.sel_idx + ibase + h * istride, sm);
     if (tid == 0) {
       p.sel_nsel[r] = K;
       p.sel_cnt[size_t(r) * p.hkv + h] = 0;

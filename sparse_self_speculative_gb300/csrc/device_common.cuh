@@ -24,6 +24,24 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Asks L2 to fetch the 128-byte line holding p (no register is written; p must lie
+// inside an allocation).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
+// The block prefetches into L2 every line touched by the floats p[0 .. n), each
+// thread taking every NT-th line; every address it names lies inside that range.
+template <int NT>
+__device__ __forceinline__ void prefetch_range_l2(const float* p, long long n) {
+  if (n <= 0) return;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t a1 = a0 + uintptr_t(n) * 4u;            // one past the last byte
+  const uintptr_t first_line = a0 & ~uintptr_t(127);
+  for (uintptr_t a = first_line + uintptr_t(threadIdx.x) * 128u; a < a1; a += uintptr_t(NT) * 128u)
+    prefetch_l2(reinterpret_cast<const void*>(a < a0 ? a0 : a));
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

@@ -86,6 +86,22 @@ __device__ __forceinline__ void average_block(const float* lg, int L, int rows, 
   }
 }
 
+// Prefetches into L2 the logit lines of positions [t0, t1) of `rows` rows (row stride
+// L, first row at lg).  Each row's range is named through its positions t0, t0 + 32,
+// ... and t1 - 1: consecutive named positions are one 128-byte line apart, and t1 - 1
+// names the last line, so every line the range spans is fetched and no address leaves
+// the range.
+template <int NT>
+__device__ __forceinline__ void prefetch_pass(const float* lg, int L, int rows, int t0, int t1) {
+  const int n = t1 - t0;
+  if (n <= 0) return;
+  const int m = (n + 31) / 32 + 1;   // named positions per row
+  for (int i = threadIdx.x; i < rows * m; i += NT) {
+    const int row = i / m, k = i - row * m;
+    prefetch_l2(lg + size_t(row) * L + (k < m - 1 ? t0 + 32 * k : t1 - 1));
+  }
+}
+
 // Counts, in s_hist, digit (u >> shift) & (nbins-1) of every key u of U[0..L) whose
 // bits under `mask` equal `prefix`.
 template <int NT>
@@ -141,7 +157,7 @@ __device__ void find_digit(const uint32_t* s_hist, int nbins, int kr, int* s_war
 // order, the two lower digits are found among their keys in shared memory, and the
 // result is filtered out of that ordered list.  kr is the rank of the K-th largest
 // key among the keys whose top digit is d1.
-template <int NT>
+template <int NT, int KW>
 __device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int kr, int ncand, int32_t* out,
                                      const TopkSmem& sm) {
   constexpr int kSeg = NT * 32;   // positions per collection segment: one ballot word per thread
@@ -149,15 +165,15 @@ __device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int 
   int run = 0;
   for (int seg0 = 0; seg0 < L; seg0 += kSeg) {
     const int nwords = (min(kSeg, L - seg0) + 31) / 32;
-    for (int w0 = warp * kWords; w0 < nwords; w0 += (NT / 32) * kWords) {
-      uint32_t u[kWords];
+    for (int w0 = warp * KW; w0 < nwords; w0 += (NT / 32) * KW) {
+      uint32_t u[KW];
 #pragma unroll
-      for (int i = 0; i < kWords; ++i) {
+      for (int i = 0; i < KW; ++i) {
         const int t = seg0 + (w0 + i) * 32 + lane;
         u[i] = (w0 + i < nwords && t < L) ? __ldcg(U + t) : 0u;
       }
 #pragma unroll
-      for (int i = 0; i < kWords; ++i) {
+      for (int i = 0; i < KW; ++i) {
         const int t = seg0 + (w0 + i) * 32 + lane;
         const unsigned m = __ballot_sync(0xffffffffu, w0 + i < nwords && t < L && (u[i] >> 21) >= d1);
         if (lane == 0 && w0 + i < nwords) sm.gt[w0 + i] = m;
@@ -231,12 +247,16 @@ __device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int 
 
 // Top-K of S[0..L) (fp32, >= 0) into out[0..K), ascending by position; equal keys go
 // to the lower position.  `ghist` holds the histogram of the top 11 bits of all L keys;
-// it is read and cleared here.
-template <int NT>
+// it is read and cleared here.  KW ballot words per warp are loaded at a time in the
+// candidate pass (registers against round trips; the result does not depend on it).
+// PREFETCH first asks L2 for all of S (for averages written long enough ago, by other
+// CTAs, to have left it).
+template <int NT, int KW = kWords, bool PREFETCH = false>
 __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, int32_t* out, const TopkSmem& sm) {
   constexpr int kSeg = NT * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
+  if (PREFETCH) prefetch_range_l2<NT>(S, L);
   // digit 1 (bits 31..21) from the accumulated histogram
   for (int b = tid; b < kSelBins; b += NT) {
     sm.hist[b] = __ldcg(ghist + b);
@@ -250,7 +270,7 @@ __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, in
   const int ncand = sm.misc[1] + int(sm.hist[sm.misc[0]]);   // keys with top digit >= the K-th's
   __syncthreads();
   if (ncand <= sm.cap) {
-    topk_from_candidates<NT>(U, L, prefix >> 21, kr, ncand, out, sm);
+    topk_from_candidates<NT, KW>(U, L, prefix >> 21, kr, ncand, out, sm);
     return;
   }
   // digits 2 (bits 20..10) and 3 (bits 9..0) by two more passes over S
