@@ -160,11 +160,15 @@ __device__ void find_digit(const uint32_t* s_hist, int nbins, int kr, int* s_war
 template <int NT, int KW>
 __device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int kr, int ncand, int32_t* out,
                                      const TopkSmem& sm) {
-  constexpr int kSeg = NT * 32;   // positions per collection segment: one ballot word per thread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Ballot words ("top digit >= d1" bits of 32 positions) of up to sm.cap words at a
+  // time go to the key array, free until the keys are gathered; one block scan then
+  // gives each thread the output offset of its contiguous run of words.
+  uint32_t* words = sm.key;
+  const int seg_pos = sm.cap * 32;
   int run = 0;
-  for (int seg0 = 0; seg0 < L; seg0 += kSeg) {
-    const int nwords = (min(kSeg, L - seg0) + 31) / 32;
+  for (int seg0 = 0; seg0 < L; seg0 += seg_pos) {
+    const int nwords = (min(seg_pos, L - seg0) + 31) / 32;
     for (int w0 = warp * KW; w0 < nwords; w0 += (NT / 32) * KW) {
       uint32_t u[KW];
 #pragma unroll
@@ -176,18 +180,24 @@ __device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int 
       for (int i = 0; i < KW; ++i) {
         const int t = seg0 + (w0 + i) * 32 + lane;
         const unsigned m = __ballot_sync(0xffffffffu, w0 + i < nwords && t < L && (u[i] >> 21) >= d1);
-        if (lane == 0 && w0 + i < nwords) sm.gt[w0 + i] = m;
+        if (lane == 0 && w0 + i < nwords) words[w0 + i] = m;
       }
     }
     __syncthreads();
-    uint32_t wb = tid < nwords ? sm.gt[tid] : 0u;
+    const int wpt = (nwords + NT - 1) / NT;
+    const int a0 = min(nwords, tid * wpt), a1 = min(nwords, a0 + wpt);
+    int c = 0;
+    for (int w = a0; w < a1; ++w) c += __popc(words[w]);
     int tot;
-    int at = run + block_exclusive_scan<NT>(__popc(wb), sm.warp, &tot);
-    while (wb) {
-      const int bit = __ffs(wb) - 1;
-      if (at < sm.cap) sm.pos[at] = seg0 + tid * 32 + bit;
-      ++at;
-      wb &= wb - 1u;
+    int at = run + block_exclusive_scan<NT>(c, sm.warp, &tot);
+    for (int w = a0; w < a1; ++w) {
+      uint32_t wb = words[w];
+      while (wb) {
+        const int bit = __ffs(wb) - 1;
+        if (at < sm.cap) sm.pos[at] = seg0 + w * 32 + bit;
+        ++at;
+        wb &= wb - 1u;
+      }
     }
     run += tot;
     __syncthreads();
@@ -257,10 +267,21 @@ __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, in
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t* U = reinterpret_cast<const uint32_t*>(S);
   if (PREFETCH) prefetch_range_l2<NT>(S, L);
-  // digit 1 (bits 31..21) from the accumulated histogram
-  for (int b = tid; b < kSelBins; b += NT) {
-    sm.hist[b] = __ldcg(ghist + b);
-    ghist[b] = 0u;
+  // digit 1 (bits 31..21) from the accumulated histogram, kPer loads in flight a thread
+  // (one for the 512-thread selection kernel, whose registers are spoken for)
+  {
+    constexpr int kPer = NT >= 512 ? 1 : (kSelBins + NT - 1) / NT;
+    for (int b0 = tid; b0 < kSelBins; b0 += kPer * NT) {
+      uint32_t v[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) v[i] = b0 + i * NT < kSelBins ? __ldcg(ghist + b0 + i * NT) : 0u;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (b0 + i * NT < kSelBins) {
+          sm.hist[b0 + i * NT] = v[i];
+          ghist[b0 + i * NT] = 0u;
+        }
+    }
   }
   __syncthreads();
   int kr = K;
