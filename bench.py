@@ -424,9 +424,78 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(clk_lo, clk_hi),
         "bytes_per_step": {"kv": acc["kv_bytes"], "fused_total": acc["fused_bytes"], "select": acc["select_bytes"]},
     }
+    if not args.no_offload:
+        result["kv_offload"] = kv_offload_context(st)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(st, seconds=args.cpu_seconds)
     return result
+
+
+# The pages' offload need: 18 MB of new KV per decode step of a 128-request
+# Qwen3-8B batch at about 10 ms per step (Dynamic KV-cache management, paper Sec. 4.4).
+OFFLOAD_NEED_GBS = 18.0
+OFFLOAD_NEED_MB_PER_STEP = 18.0
+OFFLOAD_STEP_MS = 10.0
+
+
+def kv_offload_context(st, n_pages: int = 4096, reps: int = 5):
+    """GB/s of sspec_kv_offload / sspec_kv_reload moving n_pages scattered physical
+    pages of the step's own cache (K and V) to and from page-locked host memory,
+    beside the copy engine's contiguous cudaMemcpyAsync of the same bytes."""
+    import numpy as np
+    import torch
+
+    import sparse_self_speculative_gb300 as ss
+
+    wl, dkv = st.wl, st.dkv
+    used = np.flatnonzero(wl.page_req >= 0)
+    n = int(min(n_pages, used.size))
+    pages = torch.from_numpy(np.random.default_rng(7).permutation(used)[:n].astype(np.int32)).cuda()
+    hkv = wl.num_kv_heads
+    hk = torch.empty((n, hkv, 16, 128), dtype=torch.int16).pin_memory()
+    hv = torch.empty((n, hkv, 16, 128), dtype=torch.int16).pin_memory()
+    dev = torch.empty((n, hkv, 16, 128), dtype=torch.int16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nbytes = 2 * hk.numel() * hk.element_size()
+    stream = torch.cuda.current_stream()
+
+    def timed(f):
+        for _ in range(2):
+            f()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            f()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    off_ms = timed(lambda: ss.sspec_kv_offload(st.shape, dkv.k, dkv.v, wl.num_pages, pages, n, hk, hv, err))
+    # reload writes the same bits back into the same pages: the cache is unchanged
+    re_ms = timed(lambda: ss.sspec_kv_reload(st.shape, dkv.k, dkv.v, wl.num_pages, pages, n, hk, hv, err))
+
+    def ce_d2h():
+        hk.copy_(dev, non_blocking=True)
+        hv.copy_(dev, non_blocking=True)
+
+    def ce_h2d():
+        dev.copy_(hk, non_blocking=True)
+        dev.copy_(hv, non_blocking=True)
+    ce_d2h_ms, ce_h2d_ms = timed(ce_d2h), timed(ce_h2d)
+    assert int(err.item()) == 0
+    off_gbs = nbytes / (off_ms / 1e3) / 1e9
+    re_gbs = nbytes / (re_ms / 1e3) / 1e9
+    return {
+        "pages": n, "bytes": nbytes,
+        "offload_gbs": off_gbs, "reload_gbs": re_gbs,
+        "copy_engine_contiguous_d2h_gbs": nbytes / (ce_d2h_ms / 1e3) / 1e9,
+        "copy_engine_contiguous_h2d_gbs": nbytes / (ce_h2d_ms / 1e3) / 1e9,
+        "need_gbs": OFFLOAD_NEED_GBS,
+        "offload_ms_for_18MB": OFFLOAD_NEED_MB_PER_STEP / 1e3 / off_gbs * 1e3,
+        "offload_share_of_10ms_step": OFFLOAD_NEED_MB_PER_STEP / 1e3 / off_gbs / (OFFLOAD_STEP_MS / 1e3),
+        "kernel": "kv_copy_kernel (scattered pages <-> page-locked host memory, one pass)",
+    }
 
 
 def cpu_baseline(st, seconds: float = 15.0, n_verify: int = 2, n_draft: int = 16):
@@ -661,6 +730,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-offload", action="store_true", help="skip the KV offload / reload context timing")
     ap.add_argument("--batch", type=int, default=0, help="first N requests of the workload (profiling cases)")
     ap.add_argument("--select", default="fused", choices=["fused", "separate"],
                     help="pillar selection inside the fused launch, or as its own launch after it")

@@ -63,7 +63,7 @@ enum {
 
 /* Bits of the device error word (int32 at byte 0 of the workspace). */
 enum {
-  SSPEC_DEVERR_PAGE_OOB = 1,        /* block-table entry outside [0, num_pages) */
+  SSPEC_DEVERR_PAGE_OOB = 1,        /* block-table or page-list entry outside [0, num_pages) */
   SSPEC_DEVERR_INDEX_OOB = 2,       /* pillar index outside [0, sel_len) */
   SSPEC_DEVERR_LENGTH = 4,          /* seq_len / sel_len / nsel inconsistent or too long */
   SSPEC_DEVERR_RANGE = 8,           /* logit / index range of a request too small */
@@ -268,6 +268,62 @@ int sspec_fused_step_select(const sspec_shape* shape, const sspec_paged_kv* kv, 
  *   bucket_out  host int32 [n_new]
  */
 int sspec_assign_buckets(int32_t k, int32_t* counts, int32_t n_new, int32_t* bucket_out);
+
+/*
+ * KV-cache offload to host memory and reload
+ * (Dynamic KV-cache management: rather than predicting output lengths, the
+ * scheduler fills GPU memory with KV cache and moves the cache of requests that
+ * no longer fit to host memory asynchronously, one chunk at a time, offloading
+ * and loading back in FIFO order; paper Sec. 4.4.  The pages put the need at
+ * about 18 GB/s: 18 MB of new KV per decode step of a 128-request Qwen3-8B
+ * batch at about 10 ms per step).
+ *
+ * sspec_kv_offload copies pages[0 .. n_pages) of the K and V caches, in list
+ * order, to host_k and host_v; sspec_kv_reload copies host_k / host_v back into
+ * the pages listed (any physical pages, e.g. a new block-table row).  Both
+ * caches use the paged layout above, so one page of one cache is
+ * page_bytes = num_kv_heads * 16 * 128 * 2 bytes, and list entry i sits at
+ * byte i * page_bytes of host_k (host_v) in the same [Hkv][16][128] layout.
+ *   k_cache, v_cache  device bf16 [num_pages][Hkv][16][128], 16-byte aligned
+ *   pages             device int32 [n_pages]; entries outside [0, num_pages)
+ *                     are skipped and set SSPEC_DEVERR_PAGE_OOB in *dev_error
+ *   host_k, host_v    page-locked host memory the device addresses directly
+ *                     (cudaHostAlloc / cudaHostRegister, e.g. PyTorch pinned
+ *                     tensors), at least n_pages * page_bytes each, 16-byte
+ *                     aligned; pageable memory is rejected (SSPEC_ERR_INVALID_ARG)
+ *   dev_error         device int32, nullable: SSPEC_DEVERR_* bits are OR-ed in
+ * A kernel moves the bytes over the host link in one pass (no staging copy):
+ * chunking is the caller's choice of the page list and host offset, and the
+ * call is asynchronous on `stream`.  n_pages == 0 enqueues nothing.
+ */
+int sspec_kv_offload(const sspec_shape* shape, const void* k_cache, const void* v_cache,
+                     int32_t num_pages, const int32_t* pages, int32_t n_pages, void* host_k,
+                     void* host_v, int32_t* dev_error, sspec_stream_t stream);
+int sspec_kv_reload(const sspec_shape* shape, void* k_cache, void* v_cache, int32_t num_pages,
+                    const int32_t* pages, int32_t n_pages, const void* host_k, const void* host_v,
+                    int32_t* dev_error, sspec_stream_t stream);
+
+/*
+ * FIFO chunk planner for offload and reload (Dynamic KV-cache management,
+ * paper Sec. 4.4: chunked transfers in FIFO order for fairness).  Host only,
+ * not thread-safe.  Requests are pushed whole (request id, page count); chunks
+ * come out oldest request first, each request's pages in order, at most
+ * max_pages per chunk; a request leaves the queue with its last chunk.
+ *   sspec_kv_fifo_create   returns NULL when out of host memory
+ *   sspec_kv_fifo_push     SSPEC_ERR_INVALID_ARG for n_pages < 1 or a null fifo
+ *   sspec_kv_fifo_next     1 and the chunk (request, first page index within the
+ *                          request, page count) when one is pending, 0 when the
+ *                          queue is empty, SSPEC_ERR_INVALID_ARG for max_pages < 1
+ *                          or null pointers
+ *   sspec_kv_fifo_pending  pages still queued (0 for a null fifo)
+ */
+typedef struct sspec_kv_fifo sspec_kv_fifo;
+sspec_kv_fifo* sspec_kv_fifo_create(void);
+void sspec_kv_fifo_destroy(sspec_kv_fifo* fifo);
+int sspec_kv_fifo_push(sspec_kv_fifo* fifo, int32_t request, int32_t n_pages);
+int sspec_kv_fifo_next(sspec_kv_fifo* fifo, int32_t max_pages, int32_t* request, int32_t* first_page,
+                       int32_t* count);
+int64_t sspec_kv_fifo_pending(const sspec_kv_fifo* fifo);
 
 /* Static English text of an SSPEC_* return code. */
 const char* sspec_error_string(int code);

@@ -8,8 +8,9 @@ shares no code with the CUDA path.
 Every function cites the passage of the paper it follows: "Accelerating
 Large-Scale Reasoning Model Inference with Sparse Self-Speculative Decoding"
 (SparseSpec), as summarised on the MLSys 2026 talk-notes page, sections
-"PillarAttn" (paper Section 4.1, Figure 7) and "Unified batch scheduler"
-(paper Section 4.2, Figure 8).
+"PillarAttn" (paper Section 4.1, Figure 7), "Unified batch scheduler"
+(paper Section 4.2, Figure 8) and "Dynamic KV-cache management" (paper
+Section 4.4; kv_offload.py).
 
 Parity pins (tests/test_oracle_pins.py): closed forms, invariants, library
 routines (PyTorch CPU scaled_dot_product_attention, scipy logsumexp) and brute
@@ -27,4 +28,9 @@ from .pillar import (  # noqa: F401
     assign_buckets,
     draft_step_of_bucket,
     fused_step,
+)
+from .kv_offload import (  # noqa: F401
+    offload_pages,
+    reload_pages,
+    fifo_chunks,
 )

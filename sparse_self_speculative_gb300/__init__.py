@@ -64,7 +64,16 @@ _SIGS = {
                                         _P, _P, _P, ctypes.c_size_t, _P]),
     "sspec_fused_step_select": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P,
                                                ctypes.c_float, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "sspec_sparse_draft_attn_noalloc": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                       ctypes.c_int64, _P, _P]),
     "sspec_assign_buckets": (ctypes.c_int, [_I32, _P, _I32, _P]),
+    "sspec_kv_offload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _P, _P]),
+    "sspec_kv_reload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _P, _P]),
+    "sspec_kv_fifo_create": (_P, []),
+    "sspec_kv_fifo_destroy": (None, [_P]),
+    "sspec_kv_fifo_push": (ctypes.c_int, [_P, _I32, _I32]),
+    "sspec_kv_fifo_next": (ctypes.c_int, [_P, _I32, _P, _P, _P]),
+    "sspec_kv_fifo_pending": (ctypes.c_int64, [_P]),
     "sspec_error_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -175,6 +184,57 @@ def sspec_fused_step_select(shape, kv, batch, k, bucket, verify_bucket, q, q_off
     _check("sspec_fused_step_select", rc)
 
 
+def sspec_sparse_draft_attn_noalloc(shape, kv, batch, q, seq_lens, sel_lens, idx, idx_off, nsel, out, lse,
+                                    total_tokens, dev_error, stream=None):
+    rc = lib().sspec_sparse_draft_attn_noalloc(ctypes.byref(shape), ctypes.byref(kv), batch, _ptr(q),
+                                               _ptr(seq_lens), _ptr(sel_lens), _ptr(idx), _ptr(idx_off),
+                                               _ptr(nsel), _ptr(out), _ptr(lse), int(total_tokens),
+                                               _ptr(dev_error), _stream(stream))
+    _check("sspec_sparse_draft_attn_noalloc", rc)
+
+
+def sspec_kv_offload(shape, k_cache, v_cache, num_pages, pages, n_pages, host_k, host_v, dev_error=None,
+                     stream=None):
+    rc = lib().sspec_kv_offload(ctypes.byref(shape), _ptr(k_cache), _ptr(v_cache), int(num_pages), _ptr(pages),
+                                int(n_pages), _ptr(host_k), _ptr(host_v), _ptr(dev_error), _stream(stream))
+    _check("sspec_kv_offload", rc)
+
+
+def sspec_kv_reload(shape, k_cache, v_cache, num_pages, pages, n_pages, host_k, host_v, dev_error=None,
+                    stream=None):
+    rc = lib().sspec_kv_reload(ctypes.byref(shape), _ptr(k_cache), _ptr(v_cache), int(num_pages), _ptr(pages),
+                               int(n_pages), _ptr(host_k), _ptr(host_v), _ptr(dev_error), _stream(stream))
+    _check("sspec_kv_reload", rc)
+
+
+def sspec_kv_fifo_create() -> int:
+    h = lib().sspec_kv_fifo_create()
+    if not h:
+        raise MemoryError("sspec_kv_fifo_create")
+    return h
+
+
+def sspec_kv_fifo_destroy(fifo: int) -> None:
+    lib().sspec_kv_fifo_destroy(fifo)
+
+
+def sspec_kv_fifo_push(fifo: int, request: int, n_pages: int) -> None:
+    _check("sspec_kv_fifo_push", lib().sspec_kv_fifo_push(fifo, request, n_pages))
+
+
+def sspec_kv_fifo_next(fifo: int, max_pages: int):
+    """The next chunk as (request, first page, count), or None when the queue is empty."""
+    r, f, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    rc = lib().sspec_kv_fifo_next(fifo, max_pages, ctypes.byref(r), ctypes.byref(f), ctypes.byref(c))
+    if rc < 0:
+        _check("sspec_kv_fifo_next", rc)
+    return (r.value, f.value, c.value) if rc == 1 else None
+
+
+def sspec_kv_fifo_pending(fifo: int) -> int:
+    return int(lib().sspec_kv_fifo_pending(fifo))
+
+
 def sspec_assign_buckets(k: int, counts, n_new: int):
     """Host call; ``counts`` is a list of k+1 ints.  Returns (buckets, new counts)."""
     c = (ctypes.c_int32 * (k + 1))(*[int(x) for x in counts])
@@ -193,5 +253,7 @@ def _nbytes(t):
 __all__ = [
     "SspecShape", "SspecPagedKV", "SspecError", "lib", "make_shape", "make_kv", "error_string",
     "sspec_workspace_size", "sspec_verify_attn", "sspec_select_pillars", "sspec_sparse_draft_attn",
-    "sspec_fused_step", "sspec_fused_step_select", "sspec_assign_buckets", "header_functions",
+    "sspec_fused_step", "sspec_fused_step_select", "sspec_sparse_draft_attn_noalloc", "sspec_assign_buckets",
+    "sspec_kv_offload", "sspec_kv_reload", "sspec_kv_fifo_create", "sspec_kv_fifo_destroy", "sspec_kv_fifo_push",
+    "sspec_kv_fifo_next", "sspec_kv_fifo_pending", "header_functions",
 ]

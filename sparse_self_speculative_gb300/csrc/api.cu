@@ -19,8 +19,6 @@ int device_sm_count() {
   return cached[dev];
 }
 
-namespace {
-
 int check_shape(const sspec_shape* s) {
   if (!s) return SSPEC_ERR_INVALID_ARG;
   if (s->head_dim != kHeadDim || s->page_size != kPage) return SSPEC_ERR_UNSUPPORTED_SHAPE;
@@ -30,6 +28,8 @@ int check_shape(const sspec_shape* s) {
   if (!(s->sm_scale > 0.f) || !std::isfinite(s->sm_scale)) return SSPEC_ERR_INVALID_ARG;
   return SSPEC_OK;
 }
+
+namespace {
 
 int check_kv(const sspec_paged_kv* kv) {
   if (!kv || !kv->k_cache || !kv->v_cache || !kv->block_table) return SSPEC_ERR_INVALID_ARG;

@@ -166,5 +166,7 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 
 int device_sm_count();
+// SSPEC_OK, or the SSPEC_ERR_* code a shape that the library cannot serve gets.
+int check_shape(const sspec_shape* s);
 
 }  // namespace sspec

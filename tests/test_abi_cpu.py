@@ -136,3 +136,58 @@ def test_fused_step_select_host_validation(lib):
     assert call(nsel=None) == ss.SSPEC_ERR_INVALID_ARG
     assert call(verify_bucket=9) == ss.SSPEC_ERR_INVALID_ARG
     assert call(batch=0) == ss.SSPEC_OK                       # nothing to do, nothing launched
+
+
+def test_kv_offload_host_validation(lib):
+    """Offload and reload reject bad shapes, null or misaligned buffers and negative
+    page counts on the host; an empty page list is a no-op.  None of these calls
+    reaches CUDA (no GPU here)."""
+    shape = ss.make_shape(16, 8)
+    for fn in (lib.sspec_kv_offload, lib.sspec_kv_reload):
+        def call(shape=shape, k=4096, v=8192, num_pages=10, pages=16, n=3, hk=1 << 20, hv=2 << 20):
+            return fn(ctypes.byref(shape) if shape is not None else None, k, v, num_pages, pages, n, hk, hv,
+                      None, None)
+        assert call(shape=None) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(shape=ss.SspecShape(16, 8, 64, 16, 0.1)) == ss.SSPEC_ERR_UNSUPPORTED_SHAPE
+        assert call(k=None) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(v=None) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(hk=None) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(hv=None) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(pages=None) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(n=-1) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(num_pages=0) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(k=4100) == ss.SSPEC_ERR_INVALID_ARG           # caches and host buffers 16-byte aligned
+        assert call(hv=(2 << 20) + 8) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(n=0, pages=None) == ss.SSPEC_OK               # empty list: nothing enqueued
+
+
+def test_kv_fifo_matches_oracle_and_rejects_bad_arguments(lib):
+    rng = np.random.default_rng(31)
+    for _ in range(40):
+        reqs = [(int(r), int(rng.integers(1, 50))) for r in rng.integers(0, 1000, size=int(rng.integers(1, 9)))]
+        m = int(rng.integers(1, 12))
+        f = ss.sspec_kv_fifo_create()
+        try:
+            for r, n in reqs:
+                ss.sspec_kv_fifo_push(f, r, n)
+            assert ss.sspec_kv_fifo_pending(f) == sum(n for _, n in reqs)
+            got = []
+            while (c := ss.sspec_kv_fifo_next(f, m)) is not None:
+                got.append(c)
+            assert got == oracle.fifo_chunks(reqs, m)
+            assert ss.sspec_kv_fifo_pending(f) == 0
+        finally:
+            ss.sspec_kv_fifo_destroy(f)
+    # pushing between chunks keeps FIFO order: the new request waits behind the old one
+    f = ss.sspec_kv_fifo_create()
+    ss.sspec_kv_fifo_push(f, 1, 5)
+    assert ss.sspec_kv_fifo_next(f, 2) == (1, 0, 2)
+    ss.sspec_kv_fifo_push(f, 2, 1)
+    assert [ss.sspec_kv_fifo_next(f, 2) for _ in range(4)] == [(1, 2, 2), (1, 4, 1), (2, 0, 1), None]
+    with pytest.raises(ss.SspecError):
+        ss.sspec_kv_fifo_push(f, 3, 0)
+    with pytest.raises(ss.SspecError):
+        ss.sspec_kv_fifo_next(f, 0)
+    ss.sspec_kv_fifo_destroy(f)
+    assert lib.sspec_kv_fifo_push(None, 1, 1) == ss.SSPEC_ERR_INVALID_ARG
+    assert lib.sspec_kv_fifo_pending(None) == 0

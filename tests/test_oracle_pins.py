@@ -340,3 +340,60 @@ def test_draft_step_of_bucket():
     for b in range(k + 1):
         seq = [oracle.draft_step_of_bucket(b, (b - 1 - i) % (k + 1), k) for i in range(k + 1)]
         assert seq == list(range(k)) + [-1]
+
+
+# --------------------------------------------------------------------------------------
+# KV-cache offload / reload and its FIFO order
+# --------------------------------------------------------------------------------------
+def test_offload_holds_each_token_row_at_its_page_and_slot():
+    """A request's host copy (its block-table pages, in order) holds token t at entry
+    t // 16, slot t % 16, for every head: checked token by token against the input
+    generator's own rows, which never go through a paged layout."""
+    wl = synth.make_workload("off", 21, 8, 4, [1, 16, 17, 90], plant="kv_per_head", plant_frac=0.05)
+    for which in ("k", "v"):
+        cache = wl.paged_cache(which)
+        for r in range(wl.batch):
+            L = int(wl.seq_lens[r])
+            npg = (L + 15) // 16
+            host = oracle.offload_pages(cache, wl.block_table[r, :npg])
+            assert host.shape == (npg, 4, 16, 128)
+            for t in range(L):
+                np.testing.assert_array_equal(host[t // 16, :, t % 16, :], wl.kv_rows(which, r, [t])[0])
+            # slots past the request's end are the cache's padding (zeros)
+            assert not host[(L - 1) // 16, :, (L - 1) % 16 + 1:, :].any()
+
+
+def test_reload_into_other_pages_round_trip_and_untouched_pages():
+    wl = synth.make_workload("rel", 22, 4, 2, [40, 33], spare_pages=5)
+    cache = wl.paged_cache("k")
+    old = wl.block_table[0, :3]
+    free = np.flatnonzero(wl.page_req < 0)[:3]
+    host = oracle.offload_pages(cache, old)
+    back = oracle.reload_pages(cache, free, host)
+    # request 0 read through its new pages is what it was
+    np.testing.assert_array_equal(oracle.paged_rows(back, free, 40), oracle.paged_rows(cache, old, 40))
+    # every page not listed keeps its bits
+    keep = np.setdiff1d(np.arange(wl.num_pages), free)
+    np.testing.assert_array_equal(back[keep], cache[keep])
+    # an out-of-range entry is skipped on both sides
+    host2 = oracle.offload_pages(cache, [old[0], wl.num_pages, -1], host_init=np.full((3, 2, 16, 128), 7, np.uint16))
+    np.testing.assert_array_equal(host2[0], cache[old[0]])
+    assert (host2[1:] == 7).all()
+    np.testing.assert_array_equal(oracle.reload_pages(cache, [wl.num_pages], host2[:1]), cache)
+
+
+def test_fifo_chunks_worked_example_and_invariants():
+    assert oracle.fifo_chunks([(7, 5), (3, 2), (9, 1)], 2) == [(7, 0, 2), (7, 2, 2), (7, 4, 1), (3, 0, 2), (9, 0, 1)]
+    assert oracle.fifo_chunks([(1, 3)], 8) == [(1, 0, 3)]
+    rng = np.random.default_rng(23)
+    for _ in range(50):
+        reqs = [(int(r), int(rng.integers(1, 40))) for r in rng.permutation(12)[: int(rng.integers(1, 8))]]
+        m = int(rng.integers(1, 10))
+        chunks = oracle.fifo_chunks(reqs, m)
+        assert all(1 <= c <= m for _, _, c in chunks)
+        # requests in queue order, each request's pages 0..n-1 exactly once, in order
+        order = [r for r, _, _ in chunks]
+        assert [r for i, r in enumerate(order) if i == 0 or order[i - 1] != r] == [r for r, _ in reqs]
+        for r, n in reqs:
+            pages = [p for rr, f, c in chunks if rr == r for p in range(f, f + c)]
+            assert pages == list(range(n))
