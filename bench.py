@@ -406,6 +406,8 @@ def run_ours(args, world, rank, local):
         "kv_gbs": kv_gbs,
         "selection": "inside the fused launch" if fused_sel else "separate launch",
         "fused_ms": f_ms, "select_ms": None if fused_sel else statistics.mean(select_ms),
+        "step_ms": dict(_dist([a.elapsed_time(b) for a, b in zip(ev_f0, ev_s1)]),
+                        what="per-step device time, event before the step's first launch to after its last"),
         f"ms_per_step_{other}_selection": other_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic,
@@ -617,6 +619,187 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------------------
+# CUDA-graph timing of the small workloads
+# --------------------------------------------------------------------------------------
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _pct(xs, p):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, max(0, int(round(p / 100.0 * (len(xs) - 1)))))]
+
+
+def _dist(ms):
+    return {"median": statistics.median(ms), "p10": _pct(ms, 10), "p90": _pct(ms, 90), "n": len(ms)}
+
+
+def run_graph(args):
+    """Workloads too small for host-issued launches, timed as CUDA-graph replays.
+
+    single_2k (one request, L = 2048): one cycle = verification of k queries with the
+    selection inside the launch, then the k sequential draft steps over the new
+    pillars (step j: pillars + j + 1 appended rows), captured as one graph.  Its
+    8 MB of K/V fits in L2, so cycles are timed warm (back to back) and cold (a
+    write of 2x L2 before each cycle, outside the timed window); cold is the figure
+    for fractions.  Other workloads: 200 fused steps with the selection inside,
+    captured in one graph and replayed."""
+    import torch
+
+    import synth
+    import sparse_self_speculative_gb300 as ss
+    from tests import harness as hz
+
+    torch.cuda.set_device(0)
+    name = args.workload
+    hq, hkv, B, k, s = synth.WORKLOADS[name]
+    G = hq // hkv
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+    row_bytes = hkv * 128 * 2 * 2
+    if name == "single_2k":
+        L = 2048
+        seed = 1000 * 1
+        # the cache also holds the k rows the draft steps append after selection
+        wl = synth.make_workload(name, seed, hq, hkv, [L + k], plant="keys_all_heads", plant_count=20,
+                                 plant_limit=L)
+        dkv = hz.DeviceKV(wl, fill="device")
+        kv = dkv.kv()
+        shape = ss.make_shape(hq, hkv)
+        K = max(1, min(L, int(math.floor(float(np.float32(s)) * L))))
+        dev = "cuda"
+        i32 = lambda a: torch.tensor(a, dtype=torch.int32, device=dev)   # noqa: E731
+        i64 = lambda a: torch.tensor(a, dtype=torch.int64, device=dev)   # noqa: E731
+        q_ver = hz.bf16_i16(wl.q_rows(0, np.arange(k))).to(dev)
+        q_dr = [hz.bf16_i16(wl.q_rows(0, np.array([k + j]))).to(dev) for j in range(k)]
+        bucket, q_off, seq_v, sel_v = i32([0]), i64([0, k]), i32([L]), i32([L])
+        loff, idx_off = i64([0, hkv * k * G * L]), i64([0, hkv * K])
+        idx = torch.zeros(hkv * K, dtype=torch.int32, device=dev)
+        nsel = torch.zeros(1, dtype=torch.int32, device=dev)
+        S = torch.empty(hkv * L, dtype=torch.float32, device=dev)
+        logits = torch.empty(hkv * k * G * L, dtype=torch.float32, device=dev)
+        out_v = torch.empty((k, hq, 128), dtype=torch.int16, device=dev)
+        lse_v = torch.empty((k, hq), dtype=torch.float32, device=dev)
+        seq_d = [i32([L + j + 1]) for j in range(k)]
+        out_d = [torch.empty((1, hq, 128), dtype=torch.int16, device=dev) for _ in range(k)]
+        lse_d = [torch.empty((1, hq), dtype=torch.float32, device=dev) for _ in range(k)]
+        ws = hz.zero_workspace(ss.sspec_workspace_size(shape, 1, k, L + k))
+
+        def cycle():
+            ss.sspec_fused_step_select(shape, kv, 1, k, bucket, 0, q_ver, q_off, seq_v, sel_v, idx, idx_off, nsel,
+                                       s, S, out_v, lse_v, logits, loff, ws)
+            for j in range(k):
+                ss.sspec_sparse_draft_attn(shape, kv, 1, q_dr[j], seq_d[j], sel_v, idx, idx_off, nsel, out_d[j],
+                                           lse_d[j], ws)
+        cycle()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cycle()
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        n = max(200, args.steps)
+        for _ in range(max(10, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        with ClockSampler(0) as clk:
+            c0 = clk.mark()
+            ev[0].record(stream)
+            for i in range(n):
+                g.replay()
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            warm = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+            cold = []
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                cold.append(e0.elapsed_time(e1))
+            c1 = clk.mark()
+        assert hz.device_error(ws) == 0
+        assert int(nsel.item()) == K
+        tokens = 2 * k
+        kv_bytes = L * row_bytes + sum((K + j + 1) * row_bytes for j in range(k))
+        dump = hkv * k * G * L * 4
+        total = kv_bytes + 2 * dump + 2 * hkv * L * 4 + hkv * K * 4 * (1 + k)
+        cold_d, warm_d = _dist(cold), _dist(warm)
+        ms = cold_d["median"]
+        achieved = total / (ms / 1e3) / 1e9
+        return {
+            "metric": METRIC, "value": tokens / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": n,
+            "warmup": max(10, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{name}: one request, Hq/Hkv {hq}/{hkv}, d 128, page 16, L {L}, k {k}, s {s} "
+                                   f"(K = {K}); a step = one cycle: verify + select, then {k} draft steps",
+                       "global_batch": 1, "parallelism": "replicas1",
+                       "l2": "cold: 2x L2 written before each timed cycle (8 MB of K/V fits in L2)",
+                       "graph": f"one CUDA graph per cycle ({1 + k} launches), replayed"},
+            "step_ms_cold": cold_d, "step_ms_warm": warm_d,
+            "warm_value": tokens / (warm_d["median"] / 1e3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "algorithmic_bytes": total,
+                         "peak_kind": peak_kind,
+                         "note": "one request: latency-bound launches, far from the bandwidth bound"},
+            "gpu_launches": (1 + k) * n, "clocks": clk.summary(c0, c1),
+            "bytes_per_step": {"kv": kv_bytes, "total": total},
+        }
+    # batched workloads: 200 fused steps with the selection inside, in one graph
+    seed = 1000 * 3
+    lens = synth.workload_lengths(name, seed)
+    wl = synth.named_workload(name, seed, seq_lens=lens)
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="setup")
+    acc = step_accounting(st)
+    S = st.score_buffer()
+    st.fused_select(S)
+    torch.cuda.synchronize()
+    per_graph = 200
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            st.fused_select(S)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = 5
+    ms = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        c0 = clk.mark()
+        for _ in range(reps):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1) / per_graph)
+        c1 = clk.mark()
+    assert hz.device_error(st.ws) == 0
+    d = _dist(ms)
+    kbytes = acc["fused_bytes"] + acc["select_bytes"]
+    achieved = kbytes / (d["median"] / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": acc["query_tokens"] / (d["median"] / 1e3), "unit": UNIT, "n_gpus": 1,
+        "steps": reps * per_graph, "warmup": 2 * per_graph, "ms_per_step": d["median"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: batch {B}, Hq/Hkv {hq}/{hkv}, d 128, page 16, k {k}, s {s}, "
+                               f"{acc['n_verify']} verify + {acc['n_draft']} draft requests",
+                   "global_batch": B, "parallelism": "replicas1",
+                   "l2": f"back to back, no flush ({kbytes / 1e9:.2f} GB read or written per step vs 129 MB of L2)",
+                   "graph": f"{per_graph} fused steps with the selection inside per CUDA graph; "
+                            f"per-step means of {reps} replays"},
+        "step_ms": d,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes": kbytes, "peak_kind": peak_kind},
+        "gpu_launches": reps * per_graph, "clocks": clk.summary(c0, c1),
+        "bytes_per_step": {"kv": acc["kv_bytes"], "fused_total": acc["fused_bytes"], "select": acc["select_bytes"]},
+    }
+
+
+# --------------------------------------------------------------------------------------
 # sweep (Qwen3-8B attention shape): sparse draft vs full decode attention, and k-query
 # verification with the dump, over context x batch x sparsity x stride
 # --------------------------------------------------------------------------------------
@@ -734,6 +917,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="first N requests of the workload (profiling cases)")
     ap.add_argument("--select", default="fused", choices=["fused", "separate"],
                     help="pillar selection inside the fused launch, or as its own launch after it")
+    ap.add_argument("--graph", action="store_true",
+                    help="CUDA-graph timing for the small workloads (single_2k cycles, or 200 fused steps)")
     ap.add_argument("--sweep", action="store_true", help="context x batch x sparsity x stride sweep (JSON lines)")
     ap.add_argument("--sweep-L", default="1024,4096,16384,65536,131072")
     ap.add_argument("--sweep-B", default="1,16,64,256")
@@ -741,6 +926,9 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)
     if args.sweep:
         return run_sweep(args)
+    if args.graph:
+        print(json.dumps(run_graph(args)))
+        return 0
     world, rank, local = dist_setup()
     if args.impl == "reference":
         if rank == 0:
