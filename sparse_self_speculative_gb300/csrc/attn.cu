@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     vchunk = t4 + td >= want ? 4 * kChunk : (t2 + td >= want ? 2 * kChunk : kChunk);
     n_draft = td;
     n_full = tf;
-    avg_passes = min(kAvgMaxPasses, max(1, ta / int(gridDim.x)));
+    avg_passes = min(avg_max_passes(kThreads), max(1, ta / int(gridDim.x)));
     const int blk = kThreads * kAvgPass * avg_passes;
     int sum = 0, an = 0;
 #pragma unroll

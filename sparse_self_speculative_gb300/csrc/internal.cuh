@@ -33,11 +33,13 @@ constexpr int kSelBins = 1 << kSelBits1;
 constexpr int kSelSegment = 16384; // positions per compaction segment
 
 // ---- selection inside the fused step ---------------------------------------------------
-// An averaging item covers 1 to kAvgMaxPasses passes of kAvgPass positions per attention
-// thread (the count is chosen per launch so that there are about as many items as
-// CTAs); a (request, kv head) has at most kMaxAvgItems of them.
+// An averaging item covers 1 to avg_max_passes(threads) passes of kAvgPass positions per
+// attention thread (the count is chosen per launch so that there are about as many items
+// as CTAs); a (request, kv head) has at most kMaxAvgItems of them.  Longer items pay the
+// per-item start and histogram flush less often; on GB300 8 passes suit the 128-thread
+// CTAs of the one-query-tile kernel and 4 the wider ones (measured).
 constexpr int kAvgPass = 8;
-constexpr int kAvgMaxPasses = 4;
+constexpr int avg_max_passes(int threads) { return threads <= 128 ? 8 : 4; }
 constexpr int kMaxAvgItems = (kMaxChunks * kChunk + 1023) / 1024;
 
 // ---- workspace layout ------------------------------------------------------------------
