@@ -544,7 +544,25 @@ def cpu_baseline(st, seconds: float = 15.0, n_verify: int = 2, n_draft: int = 16
         passes += 1
     return {"value": tokens * passes / t, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{len(v_ids)} verify + {len(d_ids)} draft requests of the step, "
-                      f"{passes} passes in {t:.1f} s (numpy float64 oracle)"}
+                      f"{passes} passes in {t:.1f} s (numpy float64 oracle)",
+            "one_thread": oracle_one_thread()}
+
+
+def oracle_one_thread(steps: int = 3):
+    """The reference arm's oracle sample timed again in a child process whose BLAS and
+    OpenMP pools hold one thread (set before numpy loads): the 1-thread baseline."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    try:
+        out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps",
+                              str(steps), "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
+        line = json.loads(out.stdout.strip().splitlines()[-1])
+        return {"value": line["value"], "unit": line["unit"], "cores": 1,
+                "sample": line["cpu_baseline"]["sample"] + f", {steps} timed steps"}
+    except Exception as e:   # the baseline is context: report why it is missing
+        return {"value": None, "unavailable": f"{type(e).__name__}: {e}"[:200]}
 
 
 def _blas_threads():
