@@ -16,7 +16,9 @@ world, rank, local = bench.dist_setup()
 bench.barrier(world)
 t = bench.max_over_ranks(10.0 + rank, world)
 w = bench.sum_over_ranks(100.0 * (rank + 1), world)
-print(json.dumps({"rank": rank, "world": world, "max": t, "sum": w}))
+# one file per rank: two processes printing to one pipe at once can interleave lines
+with open(os.path.join(os.environ["OUT_DIR"], f"rank{rank}.json"), "w") as f:
+    json.dump({"rank": rank, "world": world, "max": t, "sum": w}, f)
 import torch.distributed as dist
 dist.destroy_process_group()
 """
@@ -42,10 +44,10 @@ def _torchrun(script_args, port, env_extra=None, timeout=240):
 def test_two_gloo_ranks_reduce_timings(tmp_path):
     script = tmp_path / "worker.py"
     script.write_text(WORKER)
-    res = _torchrun([str(script)], 29611)
+    res = _torchrun([str(script)], 29611, env_extra={"OUT_DIR": str(tmp_path)})
     assert res.returncode == 0, res.stderr[-2000:]
     import json
-    lines = [json.loads(l) for l in res.stdout.splitlines() if l.startswith("{")]
+    lines = [json.loads((tmp_path / f"rank{r}.json").read_text()) for r in range(2)]
     assert sorted(l["rank"] for l in lines) == [0, 1]
     for l in lines:
         assert l["world"] == 2 and l["max"] == 11.0 and l["sum"] == 300.0
