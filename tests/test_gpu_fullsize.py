@@ -6,10 +6,12 @@ selection at s = 0.05 (K = 102), then 8 sparse draft steps, each appending one
 token.  Everything is compared with the oracle.
 
 The unified-batch workloads (32 requests / Qwen3-8B shape, 256 requests with
-AIME-like lengths / Qwen3-1.7B shape, 128 requests / Qwen3-14B shape) run the
-fused step and selection at full size.  Properties that hold at any size are
-checked on every request (finite outputs, averages of each head summing to 1,
-pillars ascending, in range and K of them); a sample of requests is compared
+AIME-like lengths / Qwen3-1.7B shape, 128 requests / Qwen3-14B shape) run, at
+full size, the launch bench.py times (the fused step with the selection inside)
+and, for comparison, the same step as two launches: the two agree bit for bit.
+Properties that hold at any size are checked on every request (finite outputs,
+averages of each head summing to 1, pillars ascending, in range and K of them);
+every verifying request and a seeded sample of 16 drafting ones are compared
 element by element with the oracle.
 """
 
@@ -103,6 +105,17 @@ def test_single_request_cycle_2k():
     assert hz.device_error(ws) == 0
 
 
+def _rows_from_cache(dkv, r, positions):
+    """K and V rows (float64, [n, Hkv, 128]) of request r at `positions`, read back from
+    the device caches the input generator filled (the attention path never writes them;
+    the device generator's bits equal the host generator's, which is tested).  At these
+    lengths regenerating the rows on the host would take minutes."""
+    pos = torch.as_tensor(np.asarray(positions, dtype=np.int64), device="cuda")
+    pages = dkv.block_table[r].long()[pos // 16]
+    slots = pos % 16
+    return tuple(oracle.bf16_bits_to_f64(hz.to_bits(c[pages, :, slots, :])) for c in (dkv.k, dkv.v))
+
+
 @pytest.mark.parametrize("name", ["qwen3_8b_b32", "qwen3_1p7b_b256_aime_len", "qwen3_14b_b128"])
 def test_unified_step_full_size(name):
     import sparse_self_speculative_gb300 as ss
@@ -112,19 +125,29 @@ def test_unified_step_full_size(name):
     buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
     dkv = hz.DeviceKV(wl, fill="device")
     st = hz.UnifiedStep(wl, dkv, k, s, buckets, pillars="synthetic")
-    st.fused()
-    S = torch.empty(max(1, int(st.logit_off[-1]) // (k * G)), dtype=torch.float32, device="cuda")
-    st.select(avg_scores=S)
+    S = st.score_buffer()
+    st.fused_select(S)                      # the bench's launch
     torch.cuda.synchronize()
     assert hz.device_error(st.ws) == 0
-    out_bits = hz.to_bits(st.d_out)
+    one = [hz.to_bits(st.d_out).copy(), st.d_lse.cpu().numpy().copy(), st.d_idx.cpu().numpy().copy(),
+           st.d_nsel.cpu().numpy().copy(), S.cpu().numpy().copy()]
+    S2 = st.score_buffer()
+    st.fused()                              # the same step as two launches
+    st.select(avg_scores=S2)
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0
+    two = [hz.to_bits(st.d_out), st.d_lse.cpu().numpy(), st.d_idx.cpu().numpy(), st.d_nsel.cpu().numpy(),
+           S2.cpu().numpy()]
+    for a, b in zip(one, two):
+        np.testing.assert_array_equal(a, b)
+    out_bits = one[0]
     out = oracle.bf16_bits_to_f64(out_bits)
-    lse = st.d_lse.cpu().numpy()
+    lse = one[1]
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     L = wl.seq_lens.astype(np.int64)
-    Sg = S.cpu().numpy()
-    idx = st.d_idx.cpu().numpy()
-    nsel = st.d_nsel.cpu().numpy()
+    Sg = one[4]
+    idx = one[2]
+    nsel = one[3]
     vr = np.flatnonzero(st.is_verify)
     for r in vr:                                   # properties on every verifying request
         soff = st.logit_off[r] // (k * G)
@@ -136,15 +159,15 @@ def test_unified_step_full_size(name):
         for h in range(hkv):
             got = idx[st.idx_off[r] + h * stride: st.idx_off[r] + h * stride + K]
             assert np.all(np.diff(got) > 0) and got[0] >= 0 and got[-1] < L[r]
-    # element-wise parity on a sample: the two shortest verifying requests and 8 drafts
+    # element-wise parity: every verifying request and a seeded sample of 16 drafts
     rng = np.random.default_rng(7)
-    sample_v = vr[np.argsort(L[vr])[:2]]
+    sample_v = vr
     dr = np.flatnonzero(~st.is_verify)
-    sample_d = rng.choice(dr, size=min(8, len(dr)), replace=False)
+    sample_d = rng.choice(dr, size=min(16, len(dr)), replace=False)
     for r in list(sample_v) + list(sample_d):
         rows = slice(st.q_off[r], st.q_off[r + 1])
         if st.is_verify[r]:
-            kf, vf = st.kv_f64(r, np.arange(int(L[r])))
+            kf, vf = _rows_from_cache(dkv, int(r), np.arange(int(L[r])))
             o_ref, l_ref, lg_ref = oracle.verify_attention(st.q_f64(r), kf, vf, hz.SCALE)
             soff = st.logit_off[r] // (k * G)
             Sr = Sg[soff: soff + hkv * L[r]].reshape(hkv, L[r]).astype(np.float64)
@@ -160,7 +183,7 @@ def test_unified_step_full_size(name):
             need = np.unique(np.concatenate(list(st.pillars[int(r)]) + [np.arange(int(st.sel_lens[r]), int(L[r]))]))
             kf = np.zeros((int(L[r]), hkv, 128))
             vf = np.zeros((int(L[r]), hkv, 128))
-            kf[need], vf[need] = st.kv_f64(r, need)
+            kf[need], vf[need] = _rows_from_cache(dkv, int(r), need)
             o_ref, l_ref = oracle.sparse_draft_attention(st.q_f64(r)[0], kf, vf, st.pillars[int(r)],
                                                          int(st.sel_lens[r]), hz.SCALE)
             o_ref, l_ref = o_ref[None], l_ref[None]
