@@ -39,7 +39,7 @@ constexpr int kSelSegment = 16384; // positions per compaction segment
 // per-item start and histogram flush less often; on GB300 8 passes suit the 128-thread
 // CTAs of the one-query-tile kernel and 4 the wider ones (measured).
 constexpr int kAvgPass = 8;
-constexpr int avg_max_passes(int threads) { return threads <= 128 ? 8 : 4; }
+__host__ __device__ constexpr int avg_max_passes(int threads) { return threads <= 128 ? 8 : 4; }
 constexpr int kMaxAvgItems = (kMaxChunks * kChunk + 1023) / 1024;
 
 // ---- workspace layout ------------------------------------------------------------------

@@ -21,6 +21,7 @@ namespace sspec {
 namespace sel {
 
 constexpr int kWords = 8;       // ballot words a warp builds per round of loads
+constexpr float kLog2eAvg = 1.4426950408889634f;   // log2(e)
 
 // Shared memory handed to the Top-K routines.
 struct TopkSmem {
@@ -67,9 +68,10 @@ __device__ __forceinline__ void average_block(const float* lg, int L, int rows, 
     }
 #pragma unroll
     for (int i = 0; i < RG; ++i) {
-      const float l = s_lse[r0 + i];
+      // exp(v - lse) as 2^(v log2 e - lse log2 e): one FMA and the hardware exp2
+      const float l2 = s_lse[r0 + i] * kLog2eAvg;
 #pragma unroll
-      for (int j = 0; j < PER; ++j) acc[j] += expf(v[i][j] - l);
+      for (int j = 0; j < PER; ++j) acc[j] += exp2f(fmaf(v[i][j], kLog2eAvg, -l2));
     }
   }
 #pragma unroll
