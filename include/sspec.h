@@ -275,8 +275,9 @@ int sspec_assign_buckets(int32_t k, int32_t* counts, int32_t n_new, int32_t* buc
  * scheduler fills GPU memory with KV cache and moves the cache of requests that
  * no longer fit to host memory asynchronously, one chunk at a time, offloading
  * and loading back in FIFO order; paper Sec. 4.4.  The pages put the need at
- * about 18 GB/s: 18 MB of new KV per decode step of a 128-request Qwen3-8B
- * batch at about 10 ms per step).
+ * about 18 GB/s for a 128-request Qwen3-8B batch, from 18 MB of new KV per
+ * decode step at about 10 ms per step; those two figures give 1.8 GB/s, so
+ * 18 GB/s is the conservative reading).
  *
  * sspec_kv_offload copies pages[0 .. n_pages) of the K and V caches, in list
  * order, to host_k and host_v; sspec_kv_reload copies host_k / host_v back into
