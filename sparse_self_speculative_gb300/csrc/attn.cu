@@ -234,7 +234,7 @@ __device__ int next_task(const AttnParams& p, long long total, uint32_t total_av
                          long long& pending, uint32_t* item) {
   const bool sel = total_avg > 0;
   unsigned long long t0 = 0;
-  unsigned sleep_ns = 128;
+  unsigned sleep_ns = 64;
   for (;;) {
     if (sel) {
       if (pending < 0 && pending != -2 &&
@@ -259,7 +259,8 @@ __device__ int next_task(const AttnParams& p, long long total, uint32_t total_av
       continue;
     }
     if (!sel || pending == -2) return 0;
-    // only a claimed, not yet published averaging slot is left: wait for it
+    // only a claimed, not yet published averaging slot is left: wait for it (each CTA
+    // polls its own slot, so short sleeps cost little and a published item starts soon)
     const unsigned long long now = global_ns();
     if (t0 == 0) {
       t0 = now;
@@ -268,7 +269,7 @@ __device__ int next_task(const AttnParams& p, long long total, uint32_t total_av
       return 0;
     }
     __nanosleep(sleep_ns);
-    sleep_ns = sleep_ns < 8192 ? sleep_ns * 2 : 8192;
+    sleep_ns = sleep_ns < 256 ? sleep_ns * 2 : 256;
   }
 }
 
