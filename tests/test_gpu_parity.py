@@ -391,7 +391,8 @@ def test_select_ties_go_to_lower_positions(L):
         np.testing.assert_array_equal(got, np.arange(K))     # all of [0, L-k] tie; lowest win
 
 
-@pytest.mark.parametrize("L,s", [(12000, 0.05), (30000, 0.2), (30000, 0.4), (40960, 0.05)])
+@pytest.mark.parametrize("L,s", [(12000, 0.05), (30000, 0.2), (30000, 0.4), (40960, 0.05),
+                                 (3000, 1.0), (12000, 1.0), (12000, 0.01)])   # s = 1: K = L
 def test_select_candidate_list_and_multipass_paths(L, s):
     """Top-K through both selection paths: the keys at or above the K-th largest key's
     top radix digit fit the shared-memory candidate list (short rows, small s), or do
@@ -424,6 +425,9 @@ def test_device_generator_matches_host():
     (40, 8, 0.05, [9000]),
     # K = 8,000 and 12,000 exceed the fused path's candidate list: its multi-pass Top-K
     (16, 8, 0.4, [20000, 30000]),
+    # the sweep's extremes: every position kept (K = L), and K = 1 for the 40-token request
+    (16, 8, 1.0, [9000]),
+    (16, 8, 0.01, [9000]),
 ])
 def test_fused_select_equals_separate_launches_bitwise(hq, hkv, s, long_lens):
     """Selection inside the fused launch writes exactly what the fused step followed by
