@@ -1,6 +1,6 @@
 """Parity at the benchmark sizes, in the launch configuration bench.py times.
 
-Config 1 (one request, 2,048 tokens, Qwen3-1.7B attention shape) runs the whole
+The single-request workload (2,048 tokens, Qwen3-1.7B attention shape) runs the whole
 PillarAttn cycle: verification of 8 causal queries with the dump, pillar
 selection at s = 0.05 (K = 102), then 8 sparse draft steps, each appending one
 token.  Everything is compared with the oracle.
