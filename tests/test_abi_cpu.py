@@ -191,3 +191,38 @@ def test_kv_fifo_matches_oracle_and_rejects_bad_arguments(lib):
     ss.sspec_kv_fifo_destroy(f)
     assert lib.sspec_kv_fifo_push(None, 1, 1) == ss.SSPEC_ERR_INVALID_ARG
     assert lib.sspec_kv_fifo_pending(None) == 0
+
+
+def test_binding_signatures_match_the_header():
+    """Every function include/sspec.h declares is bound with as many arguments as its
+    prototype lists (a stale ctypes signature would pass garbage through the ABI)."""
+    import re
+    text = open(ss.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(sspec_\w+)\s*\(([^;{]*?)\)\s*;", text):
+        args = m.group(2).strip()
+        protos[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    assert set(protos) == set(ss.header_functions())
+    for name, n in protos.items():
+        assert name in ss._SIGS, name
+        assert len(ss._SIGS[name][1]) == n, (name, len(ss._SIGS[name][1]), n)
+
+
+def test_reference_arm_json_line_has_the_contract_keys():
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
