@@ -47,20 +47,29 @@ def source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) over all algorithmic bytes
+# of one fused launch, from an ncu capture of the 48-request case of the same length
+# distribution (the 256-request case holds about 16 GB on the device, too much for a
+# multi-pass capture).  The bench line scales it to the full launch and reports it only
+# while the kernel sources are the ones the capture was taken on.
+TRAFFIC_CAPTURE = {
+    "source_sha256_prefix": "2f3bbb9e9cc4453d",
+    "ratio_with_selection": 0.966,
+    "ratio_attention_only": 0.985,
+    "capture": "ncu dram__bytes_read.sum + dram__bytes_write.sum, 2 launches of the 48-request case "
+               "(profiles/attn_persistent_qwen3_1p7b_b48.md), scaled to this launch's algorithmic bytes",
+}
+
+
 def _traffic_ratio(with_selection: bool):
     """DRAM traffic / algorithmic bytes of the fused launch (with or without the
-    selection inside it) from the committed ncu summary, if that was taken on the
-    current sources; else None."""
-    prof = os.path.join(ROOT, "profiles", "attn_persistent_qwen3_1p7b_b48.md")
-    key = "traffic_ratio_with_selection:" if with_selection else "traffic_ratio:"
-    try:
-        text = open(prof).read()
-        ratio = float(text.split(key)[1].split()[0])
-        if text.split("source_sha256_prefix:")[1].split()[0] != source_sha():
-            return None
-        return ratio
-    except Exception:
+    selection inside it) if the capture was taken on the current sources; else None."""
+    if TRAFFIC_CAPTURE["source_sha256_prefix"] != source_sha():
         return None
+    return TRAFFIC_CAPTURE["ratio_with_selection" if with_selection else "ratio_attention_only"]
+
+
+SPEC_HBM_GBS = 8000.0   # the ~8 TB/s HBM3e figure the problem statement names
 
 
 def _peaks():
@@ -387,12 +396,15 @@ def run_ours(args, world, rank, local):
 
     peak, peak_kind = _peaks()
     f_ms = statistics.mean(fused_ms)
-    # the dominant kernel: the fused launch (with the selection when it runs inside it)
+    # the dominant kernel: the fused launch (with the selection when it runs inside it).
+    # Its algorithmic bytes are the K and V bytes (every row once); the bytes of the
+    # dump, the selection, queries, outputs and indices are reported beside them.
     kbytes = acc["fused_bytes"] + (acc["select_bytes"] if fused_sel else 0)
-    achieved = kbytes / (f_ms / 1e3) / 1e9
+    all_gbs = kbytes / (f_ms / 1e3) / 1e9
     ratio = _traffic_ratio(fused_sel)
     traffic = None if ratio is None else kbytes * ratio
     kv_gbs = acc["kv_bytes"] / (f_ms / 1e3) / 1e9
+    total_gbs = acc["fused_bytes"] / (f_ms / 1e3) / 1e9
     gpu_launches = (1 if fused_sel else 2) * args.steps
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -409,11 +421,20 @@ def run_ours(args, world, rank, local):
         "step_ms": dict(_dist([a.elapsed_time(b) for a, b in zip(ev_f0, ev_s1)]),
                         what="per-step device time, event before the step's first launch to after its last"),
         f"ms_per_step_{other}_selection": other_ms,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": kv_gbs, "peak": peak, "unit": "GB/s", "frac": kv_gbs / peak,
                      "traffic": traffic,
+                     "traffic_note": (TRAFFIC_CAPTURE["capture"] + "; DRAM bytes of all the launch's traffic")
+                     if traffic is not None else "null: no ncu capture taken on the current kernel sources",
                      "kernel": "attn_persistent (fused step" + (" with selection)" if fused_sel else ")"),
-                     "algorithmic_bytes": kbytes, "peak_kind": peak_kind,
-                     "kv_gbs": kv_gbs, "kv_frac": kv_gbs / peak},
+                     "algorithmic_bytes": acc["kv_bytes"],
+                     "algorithmic": "K and V bytes, every row read once (verify: all L rows; draft: K + j + 1 rows)",
+                     "peak_kind": peak_kind,
+                     "kv_gbs": kv_gbs, "kv_frac": kv_gbs / peak, "kv_frac_of_8tbs_spec": kv_gbs / SPEC_HBM_GBS,
+                     "total_bytes": acc["fused_bytes"], "total_gbs": total_gbs, "total_frac": total_gbs / peak,
+                     "total_note": "K/V + logit dump writes + q/out/lse + pillar indices + block table",
+                     "all_bytes": kbytes, "all_gbs": all_gbs, "all_frac": all_gbs / peak,
+                     "all_note": "total bytes plus, with the selection inside, the dump read-back, the "
+                                 "averages written and re-read, and the pillars written"},
         "roofline_attention_only": {
             "kernel": "attn_persistent (fused step without selection)", "ms": attn_only_ms,
             "achieved": acc["fused_bytes"] / (attn_only_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
@@ -819,13 +840,170 @@ def run_graph(args):
 
 
 # --------------------------------------------------------------------------------------
+# the pages' kernel-level comparison: the fused kernel against sequential launches and
+# against naive batching (talk notes, "Unified batch scheduler", fused attention kernel;
+# paper Sec. 5.6, Fig. 15: 1.3x and 1.8x on H100, context only)
+# --------------------------------------------------------------------------------------
+PAGES_FUSED_VS_SEQUENTIAL = 1.3
+PAGES_FUSED_VS_NAIVE = 1.8
+
+
+def run_compare(args):
+    """On the bench workload, times (iii) the fused step (one launch) against (i) the
+    same work as sequential launches (sspec_verify_attn over the verifying requests,
+    then sspec_sparse_draft_attn over the drafting ones) and (ii) naive batching, read
+    as every request of the batch verifying with full attention (no sparse template:
+    the unified batch run through the verify path alone).  Each also with the pillar
+    selection of its verifying requests (inside the fused launch; its own launch
+    otherwise).  All inputs are resident and larger than L2."""
+    import torch
+
+    import synth
+    import sparse_self_speculative_gb300 as ss
+    from tests import harness as hz
+
+    torch.cuda.set_device(0)
+    name = args.workload
+    hq, hkv, B, k, s = synth.WORKLOADS[name]
+    G = hq // hkv
+    seed = 1000 * 3
+    lens = synth.workload_lengths(name, seed)
+    if args.batch:
+        lens = lens[:args.batch]
+        B = len(lens)
+    wl = synth.named_workload(name, seed, seq_lens=lens)
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="setup")
+    acc = step_accounting(st)
+    shape, dev = st.shape, "cuda"
+    S_fused = st.score_buffer()
+    L = wl.seq_lens.astype(np.int64)
+    t64 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).to(dev)   # noqa: E731
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)   # noqa: E731
+
+    # (i) sequential launches: the verifying and the drafting requests as batches of their own
+    vr, dr = np.flatnonzero(st.is_verify), np.flatnonzero(~st.is_verify)
+    nv, nd = len(vr), len(dr)
+    qrows_v = np.concatenate([np.arange(st.q_off[r], st.q_off[r + 1]) for r in vr])
+    q_v = st.d_q[t64(qrows_v)].contiguous()
+    kv_v = ss.make_kv(dkv.k, dkv.v, dkv.block_table[t64(vr)].contiguous())
+    seq_v = t32(L[vr])
+    loff_v = np.zeros(nv + 1, dtype=np.int64)
+    loff_v[1:] = np.cumsum(hkv * k * G * L[vr])
+    d_loff_v = t64(loff_v)
+    logits_v = torch.empty(int(loff_v[-1]), dtype=torch.float32, device=dev)
+    out_v = torch.empty((nv, k, hq, 128), dtype=torch.int16, device=dev)
+    lse_v = torch.empty((nv, k, hq), dtype=torch.float32, device=dev)
+    K_v = np.array([hz._pillar_count(s, int(x)) for x in L[vr]], dtype=np.int64)
+    ioff_v = np.zeros(nv + 1, dtype=np.int64)
+    ioff_v[1:] = np.cumsum(hkv * K_v)
+    idx_v = torch.empty(int(ioff_v[-1]), dtype=torch.int32, device=dev)
+    d_ioff_v = t64(ioff_v)
+    nsel_v = torch.empty(nv, dtype=torch.int32, device=dev)
+    S_v = torch.empty(int(hkv * L[vr].sum()), dtype=torch.float32, device=dev)
+    ws_v = hz.zero_workspace(ss.sspec_workspace_size(shape, nv, k, int(L[vr].sum())))
+    q_d = st.d_q[t64(st.q_off[dr])].contiguous()
+    kv_d = ss.make_kv(dkv.k, dkv.v, dkv.block_table[t64(dr)].contiguous())
+    seq_d, sel_d = t32(L[dr]), t32(st.sel_lens[dr])
+    idx_rows = np.concatenate([np.arange(st.idx_off[r], st.idx_off[r + 1]) for r in dr])
+    idx_d = st.d_idx[t64(idx_rows)].contiguous()
+    ioff_d = np.zeros(nd + 1, dtype=np.int64)
+    ioff_d[1:] = np.cumsum(st.idx_off[dr + 1] - st.idx_off[dr])
+    d_ioff_d = t64(ioff_d)
+    nsel_d = st.d_nsel[t64(dr)].contiguous()
+    out_d = torch.empty((nd, hq, 128), dtype=torch.int16, device=dev)
+    lse_d = torch.empty((nd, hq), dtype=torch.float32, device=dev)
+    tot_d = int((st.nsel_host[dr].astype(np.int64) + L[dr] - st.sel_lens[dr]).sum())
+    ws_d = hz.zero_workspace(ss.sspec_workspace_size(shape, nd, 1, tot_d))
+
+    def seq_attn():
+        ss.sspec_verify_attn(shape, kv_v, nv, k, q_v, seq_v, out_v, lse_v, logits_v, d_loff_v, ws_v)
+        ss.sspec_sparse_draft_attn(shape, kv_d, nd, q_d, seq_d, sel_d, idx_d, d_ioff_d, nsel_d, out_d, lse_d, ws_d)
+
+    def seq_select():
+        ss.sspec_verify_attn(shape, kv_v, nv, k, q_v, seq_v, out_v, lse_v, logits_v, d_loff_v, ws_v)
+        ss.sspec_select_pillars(shape, nv, k, s, logits_v, d_loff_v, lse_v, None, seq_v, S_v, idx_v, d_ioff_v,
+                                nsel_v, ws_v)
+        ss.sspec_sparse_draft_attn(shape, kv_d, nd, q_d, seq_d, sel_d, idx_d, d_ioff_d, nsel_d, out_d, lse_d, ws_d)
+
+    # (ii) naive batching: every request verifies its k queries over its whole cache
+    q_all = hz.bf16_i16(np.stack([wl.q_rows(r, np.arange(k)) for r in range(B)])).to(dev)
+    loff_a = np.zeros(B + 1, dtype=np.int64)
+    loff_a[1:] = np.cumsum(hkv * k * G * L)
+    d_loff_a = t64(loff_a)
+    logits_a = torch.empty(int(loff_a[-1]), dtype=torch.float32, device=dev)
+    out_a = torch.empty((B, k, hq, 128), dtype=torch.int16, device=dev)
+    lse_a = torch.empty((B, k, hq), dtype=torch.float32, device=dev)
+    K_a = np.array([hz._pillar_count(s, int(x)) for x in L], dtype=np.int64)
+    ioff_a = np.zeros(B + 1, dtype=np.int64)
+    ioff_a[1:] = np.cumsum(hkv * K_a)
+    idx_a = torch.empty(int(ioff_a[-1]), dtype=torch.int32, device=dev)
+    d_ioff_a = t64(ioff_a)
+    nsel_a = torch.empty(B, dtype=torch.int32, device=dev)
+    S_a = torch.empty(int(hkv * L.sum()), dtype=torch.float32, device=dev)
+    seq_a = t32(L)
+    ws_a = hz.zero_workspace(ss.sspec_workspace_size(shape, B, k, int(L.sum())))
+    kv_a = dkv.kv()
+
+    def naive_attn():
+        ss.sspec_verify_attn(shape, kv_a, B, k, q_all, seq_a, out_a, lse_a, logits_a, d_loff_a, ws_a)
+
+    def naive_select():
+        naive_attn()
+        ss.sspec_select_pillars(shape, B, k, s, logits_a, d_loff_a, lse_a, None, seq_a, S_a, idx_a, d_ioff_a,
+                                nsel_a, ws_a)
+
+    variants = {
+        "fused": (lambda: st.fused(), 1),
+        "fused_select": (lambda: st.fused_select(S_fused), 1),
+        "sequential": (seq_attn, 2),
+        "sequential_select": (seq_select, 3),
+        "naive_all_verify": (naive_attn, 1),
+        "naive_all_verify_select": (naive_select, 2),
+    }
+    stream = torch.cuda.current_stream()
+    n = max(5, args.steps)
+    res = {}
+    with ClockSampler(0) as clk:
+        c0 = clk.mark()
+        for key, (f, launches) in variants.items():
+            for _ in range(args.warmup):
+                f()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                f()
+            b.record(stream)
+            torch.cuda.synchronize()
+            res[key] = {"ms": a.elapsed_time(b) / n, "launches": launches}
+        c1 = clk.mark()
+    for ws in (st.ws, ws_v, ws_d, ws_a):
+        assert hz.device_error(ws) == 0, "device error word set"
+    fm, fsm = res["fused"]["ms"], res["fused_select"]["ms"]
+    return {
+        "compare": True, "workload": f"{name}: batch {B}, {nv} verify + {nd} draft requests, k {k}, s {s}",
+        "steps": n, "warmup": args.warmup, "variants": res,
+        "sequential_over_fused": res["sequential"]["ms"] / fm,
+        "sequential_select_over_fused_select": res["sequential_select"]["ms"] / fsm,
+        "naive_over_fused": res["naive_all_verify"]["ms"] / fm,
+        "naive_select_over_fused_select": res["naive_all_verify_select"]["ms"] / fsm,
+        "pages_context": {"fused_over_sequential": PAGES_FUSED_VS_SEQUENTIAL, "fused_over_naive": PAGES_FUSED_VS_NAIVE,
+                          "note": "H100, the pages' own kernels and batch; context, not targets"},
+        "naive_reading": "every request of the batch verifies (k queries, full attention, dump)",
+        "kv_bytes_fused": acc["kv_bytes"], "kv_bytes_naive": int(L.sum() * hkv * 128 * 2 * 2),
+        "clocks": clk.summary(c0, c1),
+    }
+
+
+# --------------------------------------------------------------------------------------
 # sweep (Qwen3-8B attention shape): sparse draft vs full decode attention, and k-query
 # verification with the dump, over context x batch x sparsity x stride
 # --------------------------------------------------------------------------------------
 def run_sweep(args):
     import torch
 
-    import oracle
     import synth
     import sparse_self_speculative_gb300 as ss
     from tests import harness as hz
@@ -892,7 +1070,7 @@ def run_sweep(args):
                 outd = torch.empty((B, hq, 128), dtype=torch.int16, device="cuda")
                 lsed = torch.empty((B, hq), dtype=torch.float32, device="cuda")
                 for s_ in S_list:
-                    nsel = np.array([oracle.pillar_count(s_, int(x)) for x in sel], dtype=np.int32)
+                    nsel = np.array([hz._pillar_count(s_, int(x)) for x in sel], dtype=np.int32)
                     ioff = np.zeros(B + 1, dtype=np.int64)
                     ioff[1:] = np.cumsum(nsel.astype(np.int64) * hkv)
                     idx = np.empty(int(ioff[-1]), dtype=np.int32)
@@ -939,12 +1117,17 @@ def main(argv=None):
     ap.add_argument("--graph", action="store_true",
                     help="CUDA-graph timing for the small workloads (single_2k cycles, or 200 fused steps)")
     ap.add_argument("--sweep", action="store_true", help="context x batch x sparsity x stride sweep (JSON lines)")
+    ap.add_argument("--compare", action="store_true",
+                    help="fused step vs sequential launches vs naive all-verify batching (one JSON line)")
     ap.add_argument("--sweep-L", default="1024,4096,16384,65536,131072")
     ap.add_argument("--sweep-B", default="1,16,64,256")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     if args.sweep:
         return run_sweep(args)
+    if args.compare:
+        print(json.dumps(run_compare(args)))
+        return 0
     if args.graph:
         print(json.dumps(run_graph(args)))
         return 0

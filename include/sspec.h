@@ -187,14 +187,17 @@ int sspec_sparse_draft_attn(const sspec_shape* shape, const sspec_paged_kv* kv, 
  *     it are rejected with SSPEC_ERR_WORKSPACE_TOO_SMALL before anything is
  *     enqueued.  total_tokens bounds the sum over requests of
  *     nsel + seq_len - sel_len.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - The first call in a CUDA context (normally: on a device) looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it for that
+ *     context; make that first call before any stream capture.
  *   - Every call on a device shares the array, which keeps the previous call's
  *     contents; each call clears the part that must start at zero with a
  *     cudaMemsetAsync on `stream`.  Calls whose work overlaps on the GPU (other
  *     streams, other host threads) race on the scratch: serialize them.
+ *     Host checks run first: a call they reject enqueues nothing.
  *   - dev_error: nullable device int32; receives this call's device error word
- *     (SSPEC_DEVERR_* bits), copied on `stream` after the kernel.
+ *     (SSPEC_DEVERR_* bits), copied on `stream` after the kernel.  A call with
+ *     batch 0 enqueues nothing and leaves it unchanged.
  * Nothing is allocated or freed and nothing synchronizes.
  */
 int sspec_sparse_draft_attn_noalloc(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
@@ -290,8 +293,11 @@ int sspec_assign_buckets(int32_t k, int32_t* counts, int32_t n_new, int32_t* buc
  *                     are skipped and set SSPEC_DEVERR_PAGE_OOB in *dev_error
  *   host_k, host_v    page-locked host memory the device addresses directly
  *                     (cudaHostAlloc / cudaHostRegister, e.g. PyTorch pinned
- *                     tensors), at least n_pages * page_bytes each, 16-byte
- *                     aligned; pageable memory is rejected (SSPEC_ERR_INVALID_ARG)
+ *                     tensors), 16-byte aligned; pageable memory is rejected
+ *                     (SSPEC_ERR_INVALID_ARG)
+ *   host_bytes        bytes available in each of host_k and host_v from the given
+ *                     addresses; a call with n_pages * page_bytes > host_bytes is
+ *                     rejected (SSPEC_ERR_INVALID_ARG) before anything is enqueued
  *   dev_error         device int32, nullable: SSPEC_DEVERR_* bits are OR-ed in
  * A kernel moves the bytes over the host link in one pass (no staging copy):
  * chunking is the caller's choice of the page list and host offset, and the
@@ -299,10 +305,10 @@ int sspec_assign_buckets(int32_t k, int32_t* counts, int32_t n_new, int32_t* buc
  */
 int sspec_kv_offload(const sspec_shape* shape, const void* k_cache, const void* v_cache,
                      int32_t num_pages, const int32_t* pages, int32_t n_pages, void* host_k,
-                     void* host_v, int32_t* dev_error, sspec_stream_t stream);
+                     void* host_v, size_t host_bytes, int32_t* dev_error, sspec_stream_t stream);
 int sspec_kv_reload(const sspec_shape* shape, void* k_cache, void* v_cache, int32_t num_pages,
                     const int32_t* pages, int32_t n_pages, const void* host_k, const void* host_v,
-                    int32_t* dev_error, sspec_stream_t stream);
+                    size_t host_bytes, int32_t* dev_error, sspec_stream_t stream);
 
 /*
  * FIFO chunk planner for offload and reload (Dynamic KV-cache management,
@@ -325,6 +331,22 @@ int sspec_kv_fifo_push(sspec_kv_fifo* fifo, int32_t request, int32_t n_pages);
 int sspec_kv_fifo_next(sspec_kv_fifo* fifo, int32_t max_pages, int32_t* request, int32_t* first_page,
                        int32_t* count);
 int64_t sspec_kv_fifo_pending(const sspec_kv_fifo* fifo);
+
+/*
+ * Reads the device error word of a workspace (Conventions above: the SSPEC_DEVERR_*
+ * bits that calls using the workspace OR-ed in; the word sits at byte 0).  The
+ * paper has no counterpart; this is the library's error channel.
+ *   workspace  device memory passed to earlier calls, 256-byte aligned
+ *   out        int32 that receives the word: device memory, page-locked host memory
+ *              (both asynchronous: read it after the stream has reached the copy) or
+ *              pageable host memory (CUDA then finishes the copy before returning)
+ *   clear      non-zero: the word is reset to 0 on `stream` after it is copied
+ * The copy is enqueued on `stream` after the work already queued there, so it sees
+ * the error bits of every call made on that stream before it.  Returns
+ * SSPEC_ERR_INVALID_ARG for null or misaligned pointers, SSPEC_ERR_CUDA if CUDA
+ * refuses the copy.
+ */
+int sspec_get_device_error(const void* workspace, int32_t* out, int32_t clear, sspec_stream_t stream);
 
 /* Static English text of an SSPEC_* return code. */
 const char* sspec_error_string(int code);

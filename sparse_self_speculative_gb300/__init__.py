@@ -67,8 +67,9 @@ _SIGS = {
     "sspec_sparse_draft_attn_noalloc": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        ctypes.c_int64, _P, _P]),
     "sspec_assign_buckets": (ctypes.c_int, [_I32, _P, _I32, _P]),
-    "sspec_kv_offload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _P, _P]),
-    "sspec_kv_reload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, _P, _P]),
+    "sspec_kv_offload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, ctypes.c_size_t, _P, _P]),
+    "sspec_kv_reload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, ctypes.c_size_t, _P, _P]),
+    "sspec_get_device_error": (ctypes.c_int, [_P, _P, _I32, _P]),
     "sspec_kv_fifo_create": (_P, []),
     "sspec_kv_fifo_destroy": (None, [_P]),
     "sspec_kv_fifo_push": (ctypes.c_int, [_P, _I32, _I32]),
@@ -193,18 +194,35 @@ def sspec_sparse_draft_attn_noalloc(shape, kv, batch, q, seq_lens, sel_lens, idx
     _check("sspec_sparse_draft_attn_noalloc", rc)
 
 
+def _host_bytes(host_k, host_v, host_bytes):
+    if host_bytes is not None:
+        return int(host_bytes)
+    if isinstance(host_k, int) or isinstance(host_v, int):
+        raise ValueError("host_bytes is required when the host buffers are raw addresses")
+    return min(_nbytes(host_k), _nbytes(host_v))
+
+
 def sspec_kv_offload(shape, k_cache, v_cache, num_pages, pages, n_pages, host_k, host_v, dev_error=None,
-                     stream=None):
+                     stream=None, host_bytes=None):
     rc = lib().sspec_kv_offload(ctypes.byref(shape), _ptr(k_cache), _ptr(v_cache), int(num_pages), _ptr(pages),
-                                int(n_pages), _ptr(host_k), _ptr(host_v), _ptr(dev_error), _stream(stream))
+                                int(n_pages), _ptr(host_k), _ptr(host_v), _host_bytes(host_k, host_v, host_bytes),
+                                _ptr(dev_error), _stream(stream))
     _check("sspec_kv_offload", rc)
 
 
 def sspec_kv_reload(shape, k_cache, v_cache, num_pages, pages, n_pages, host_k, host_v, dev_error=None,
-                    stream=None):
+                    stream=None, host_bytes=None):
     rc = lib().sspec_kv_reload(ctypes.byref(shape), _ptr(k_cache), _ptr(v_cache), int(num_pages), _ptr(pages),
-                               int(n_pages), _ptr(host_k), _ptr(host_v), _ptr(dev_error), _stream(stream))
+                               int(n_pages), _ptr(host_k), _ptr(host_v), _host_bytes(host_k, host_v, host_bytes),
+                               _ptr(dev_error), _stream(stream))
     _check("sspec_kv_reload", rc)
+
+
+def sspec_get_device_error(workspace, out, clear: bool = False, stream=None) -> None:
+    """Copies the workspace's device error word into ``out`` (an int32 tensor, device
+    or page-locked host) on the stream; ``clear`` resets the word afterwards."""
+    rc = lib().sspec_get_device_error(_ptr(workspace), _ptr(out), 1 if clear else 0, _stream(stream))
+    _check("sspec_get_device_error", rc)
 
 
 def sspec_kv_fifo_create() -> int:
@@ -255,5 +273,5 @@ __all__ = [
     "sspec_workspace_size", "sspec_verify_attn", "sspec_select_pillars", "sspec_sparse_draft_attn",
     "sspec_fused_step", "sspec_fused_step_select", "sspec_sparse_draft_attn_noalloc", "sspec_assign_buckets",
     "sspec_kv_offload", "sspec_kv_reload", "sspec_kv_fifo_create", "sspec_kv_fifo_destroy", "sspec_kv_fifo_push",
-    "sspec_kv_fifo_next", "sspec_kv_fifo_pending", "header_functions",
+    "sspec_kv_fifo_next", "sspec_kv_fifo_pending", "sspec_get_device_error", "header_functions",
 ]

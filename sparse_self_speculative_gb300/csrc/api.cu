@@ -81,7 +81,7 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
                   const int32_t* idx, const int64_t* idx_off, const int32_t* nsel, void* out,
                   float* lse, float* logits, const int64_t* logit_off, void* workspace,
                   size_t ws_bytes, sspec_stream_t stream, float sel_s = 0.f, float* sel_scores = nullptr,
-                  int32_t* sel_idx = nullptr, int32_t* sel_nsel = nullptr) {
+                  int32_t* sel_idx = nullptr, int32_t* sel_nsel = nullptr, PreLaunch pre = PreLaunch{}) {
   int rc = check_shape(shape);
   if (rc) return rc;
   if ((rc = check_kv(kv))) return rc;
@@ -151,11 +151,22 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
     p.avg_reserve = &w.hdr->avg_reserve;
     p.avg_head = &w.hdr->avg_head;
   }
-  return launch_attention(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSPEC_OK
-                                                                                     : SSPEC_ERR_CUDA;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (pre.fn && (rc = pre.fn(pre.ctx, cs)) != SSPEC_OK) return rc;
+  return launch_attention(p, cs) == cudaSuccess ? SSPEC_OK : SSPEC_ERR_CUDA;
 }
 
 }  // namespace
+
+int sparse_draft_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch, const void* q,
+                      const int32_t* seq_lens, const int32_t* sel_lens, const int32_t* idx, const int64_t* idx_off,
+                      const int32_t* nsel, void* out, float* lse, void* workspace, size_t ws_bytes,
+                      sspec_stream_t stream, PreLaunch pre) {
+  return run_attention(shape, kv, batch, 1, kAllDraft, nullptr, 0, q, nullptr, seq_lens, sel_lens, idx, idx_off,
+                       nsel, out, lse, nullptr, nullptr, workspace, ws_bytes, stream, 0.f, nullptr, nullptr, nullptr,
+                       pre);
+}
+
 }  // namespace sspec
 
 using namespace sspec;
@@ -184,8 +195,8 @@ int sspec_sparse_draft_attn(const sspec_shape* shape, const sspec_paged_kv* kv, 
                             const void* q, const int32_t* seq_lens, const int32_t* sel_lens,
                             const int32_t* idx, const int64_t* idx_off, const int32_t* nsel, void* out,
                             float* lse, void* workspace, size_t ws_bytes, sspec_stream_t stream) {
-  return run_attention(shape, kv, batch, 1, kAllDraft, nullptr, 0, q, nullptr, seq_lens, sel_lens, idx,
-                       idx_off, nsel, out, lse, nullptr, nullptr, workspace, ws_bytes, stream);
+  return sparse_draft_attn(shape, kv, batch, q, seq_lens, sel_lens, idx, idx_off, nsel, out, lse, workspace,
+                           ws_bytes, stream, PreLaunch{});
 }
 
 int sspec_fused_step(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch, int32_t k,
@@ -254,6 +265,21 @@ int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, fl
   p.cnt = w.sel_cnt;
   p.hist = w.sel_hist;
   return launch_select(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSPEC_OK : SSPEC_ERR_CUDA;
+}
+
+int sspec_get_device_error(const void* workspace, int32_t* out, int32_t clear, sspec_stream_t stream) {
+  if (!workspace || !out || !aligned(workspace, 256)) return SSPEC_ERR_INVALID_ARG;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // the error word is the first field of the workspace header
+  if (cudaMemcpyAsync(out, workspace, sizeof(int32_t), cudaMemcpyDefault, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SSPEC_ERR_CUDA;
+  }
+  if (clear && cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(int32_t), cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SSPEC_ERR_CUDA;
+  }
+  return SSPEC_OK;
 }
 
 int sspec_assign_buckets(int32_t k, int32_t* counts, int32_t n_new, int32_t* bucket_out) {

@@ -163,6 +163,20 @@ struct SelectParams {
   uint32_t* hist;             // [batch * hkv][kSelBins], zero between calls
 };
 
+// Work an entry point enqueues on its stream once its host checks have passed and
+// before its kernel (the allocation-free entry point clears its fixed scratch there);
+// returns SSPEC_OK or an SSPEC_ERR_* code that aborts the call.
+struct PreLaunch {
+  int (*fn)(void* ctx, cudaStream_t stream) = nullptr;
+  void* ctx = nullptr;
+};
+
+// sspec_sparse_draft_attn with a pre-launch step.
+int sparse_draft_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch, const void* q,
+                      const int32_t* seq_lens, const int32_t* sel_lens, const int32_t* idx, const int64_t* idx_off,
+                      const int32_t* nsel, void* out, float* lse, void* workspace, size_t ws_bytes,
+                      sspec_stream_t stream, PreLaunch pre);
+
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);

@@ -82,13 +82,17 @@ int host_buffer_address(const void* p, void** dev) {
 
 template <bool TO_HOST>
 int kv_transfer(const sspec_shape* shape, void* k_cache, void* v_cache, int32_t num_pages, const int32_t* pages,
-                int32_t n_pages, const void* host_k, const void* host_v, int32_t* dev_error, sspec_stream_t stream) {
+                int32_t n_pages, const void* host_k, const void* host_v, size_t host_bytes, int32_t* dev_error,
+                sspec_stream_t stream) {
   int rc = check_shape(shape);
   if (rc != SSPEC_OK) return rc;
   if (n_pages < 0 || num_pages < 1) return SSPEC_ERR_INVALID_ARG;
   if (!k_cache || !v_cache || !host_k || !host_v || (n_pages > 0 && !pages)) return SSPEC_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(host_k) || !aligned16(host_v))
     return SSPEC_ERR_INVALID_ARG;
+  // the kernel moves n_pages whole pages of each cache: both host buffers must hold them
+  const size_t page_bytes = size_t(shape->num_kv_heads) * kPage * kHeadDim * 2;
+  if (size_t(n_pages) * page_bytes > host_bytes) return SSPEC_ERR_INVALID_ARG;
   if (n_pages == 0) return SSPEC_OK;
   void* hk = nullptr;
   void* hv = nullptr;
@@ -121,17 +125,17 @@ struct sspec_kv_fifo {
 extern "C" {
 
 int sspec_kv_offload(const sspec_shape* shape, const void* k_cache, const void* v_cache, int32_t num_pages,
-                     const int32_t* pages, int32_t n_pages, void* host_k, void* host_v, int32_t* dev_error,
-                     sspec_stream_t stream) {
+                     const int32_t* pages, int32_t n_pages, void* host_k, void* host_v, size_t host_bytes,
+                     int32_t* dev_error, sspec_stream_t stream) {
   return sspec::kv_transfer<true>(shape, const_cast<void*>(k_cache), const_cast<void*>(v_cache), num_pages,
-                                  pages, n_pages, host_k, host_v, dev_error, stream);
+                                  pages, n_pages, host_k, host_v, host_bytes, dev_error, stream);
 }
 
 int sspec_kv_reload(const sspec_shape* shape, void* k_cache, void* v_cache, int32_t num_pages,
                     const int32_t* pages, int32_t n_pages, const void* host_k, const void* host_v,
-                    int32_t* dev_error, sspec_stream_t stream) {
-  return sspec::kv_transfer<false>(shape, k_cache, v_cache, num_pages, pages, n_pages, host_k, host_v, dev_error,
-                                   stream);
+                    size_t host_bytes, int32_t* dev_error, sspec_stream_t stream) {
+  return sspec::kv_transfer<false>(shape, k_cache, v_cache, num_pages, pages, n_pages, host_k, host_v, host_bytes,
+                                   dev_error, stream);
 }
 
 sspec_kv_fifo* sspec_kv_fifo_create(void) { return new (std::nothrow) sspec_kv_fifo(); }

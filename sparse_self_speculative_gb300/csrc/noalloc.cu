@@ -6,6 +6,7 @@
 // that must not allocate on its hot path at all.  This entry point takes the
 // same inputs and outputs as sspec_sparse_draft_attn but needs no workspace:
 // its scratch is a fixed array in this library's device memory.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -19,27 +20,82 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once per
-// device (in host code the array's name is only a host-side stand-in).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Device address of g_noalloc_scratch in the current CUDA context (in host code the
+// array's name is only a host-side stand-in).  The address is looked up once per
+// context and cached under the context's id, which CUDA never reuses within a
+// process: after cudaDeviceReset, or in another context on the same device, the
+// library's module is loaded again, possibly elsewhere, and gets its own lookup.
 void* scratch_address(int* rc) {
   static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    *rc = SSPEC_ERR_CUDA;
-    return nullptr;
-  }
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  constexpr int kSlots = 64;
+  static unsigned long long ids[kSlots] = {0};
+  static void* addrs[kSlots] = {nullptr};
+  static int used = 0;
+  *rc = SSPEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      *rc = SSPEC_ERR_CUDA;
+  if (!get_current || !get_id) {
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", reinterpret_cast<void**>(&get_current), 12000,
+                                         cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", reinterpret_cast<void**>(&get_id), 12000, cudaEnableDefault,
+                                         &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess) {
+      get_current = nullptr;
+      get_id = nullptr;
+      cudaGetLastError();
       return nullptr;
     }
-    addr[dev] = p;
   }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return nullptr;
+  if (!ctx) {
+    // no context is current yet: make the current device's primary context current
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
+  }
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return nullptr;
+  for (int i = 0; i < used; ++i)
+    if (ids[i] == id) {
+      *rc = SSPEC_OK;
+      return addrs[i];
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  const int slot = used < kSlots ? used++ : int(id % kSlots);   // beyond 64 contexts: overwrite a slot
+  ids[slot] = id;
+  addrs[slot] = p;
   *rc = SSPEC_OK;
-  return addr[dev];
+  return p;
+}
+
+// Clears, on the call's stream, the part of the scratch the draft attention needs at
+// zero: the header (error word, queue counters) and the per (request, kv head)
+// arrival counters.  Runs after the call's host checks, so a rejected call enqueues
+// nothing.
+struct ClearCtx {
+  void* scratch;
+  size_t bytes;
+};
+int clear_scratch(void* c, cudaStream_t s) {
+  const ClearCtx* cc = static_cast<const ClearCtx*>(c);
+  if (cudaMemsetAsync(cc->scratch, 0, cc->bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return SSPEC_ERR_CUDA;
+  }
+  return SSPEC_OK;
 }
 
 }  // namespace
@@ -56,15 +112,14 @@ extern "C" int sspec_sparse_draft_attn_noalloc(const sspec_shape* shape, const s
   int rc = SSPEC_OK;
   void* scratch = scratch_address(&rc);
   if (rc != SSPEC_OK) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the scratch keeps the previous call's contents: clear the error word and the
-  // counters that must start at zero
-  if (cudaMemsetAsync(scratch, 0, sspec::ws_region_offset(batch, shape->num_kv_heads), s) != cudaSuccess)
+  ClearCtx cc{scratch, sspec::kWsHeaderBytes + sspec::ws_counter_bytes(batch, shape->num_kv_heads)};
+  rc = sspec::sparse_draft_attn(shape, kv, batch, q, seq_lens, sel_lens, idx, idx_off, nsel, out, lse, scratch,
+                                kNoAllocScratchBytes, stream, sspec::PreLaunch{clear_scratch, &cc});
+  if (rc == SSPEC_OK && batch > 0 && dev_error &&
+      cudaMemcpyAsync(dev_error, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
     return SSPEC_ERR_CUDA;
-  rc = sspec_sparse_draft_attn(shape, kv, batch, q, seq_lens, sel_lens, idx, idx_off, nsel, out, lse, scratch,
-                               kNoAllocScratchBytes, stream);
-  if (rc == SSPEC_OK && dev_error &&
-      cudaMemcpyAsync(dev_error, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-    return SSPEC_ERR_CUDA;
+  }
   return rc;
 }

@@ -47,6 +47,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -84,9 +85,22 @@ def tensor_key(seed: int, tensor_id: int) -> int:
     return int(splitmix64(seed, np.array([tensor_id]))[0])
 
 
+_CHUNK = 1 << 16   # counters per pass: keeps numpy's temporaries in cache (about 10x faster)
+
+
 def normal_bf16(key: int, counters: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) of the Irwin-Hall(12) variates at ``counters``."""
     c = np.asarray(counters, dtype=np.uint64)
+    if c.size > _CHUNK:
+        flat = c.reshape(-1)
+        out = np.empty(flat.shape, dtype=np.uint16)
+        for i in range(0, flat.size, _CHUNK):
+            out[i:i + _CHUNK] = _normal_bf16(key, flat[i:i + _CHUNK])
+        return out.reshape(c.shape)
+    return _normal_bf16(key, c)
+
+
+def _normal_bf16(key: int, c: np.ndarray) -> np.ndarray:
     total = np.zeros(c.shape, dtype=np.int64)
     with np.errstate(over="ignore"):
         base = c * np.uint64(3)
@@ -159,7 +173,23 @@ class Workload:
         """uint16 [len(t), Hkv, 128] bf16 bits of logical K or V rows of request r."""
         t = np.asarray(t, dtype=np.int64)
         tid = T_K if which == "k" else T_V
-        bits = normal_bf16(tensor_key(self.seed, tid), kv_counters(r, t, self.num_kv_heads))
+        key = tensor_key(self.seed, tid)
+        bits = np.empty((t.shape[0], self.num_kv_heads, HEAD_DIM), dtype=np.uint16)
+        step = max(1, _CHUNK // (self.num_kv_heads * HEAD_DIM))   # rows per pass
+
+        def rows(i):
+            sl = t[i:i + step]
+            bits[i:i + step] = _normal_bf16(key, kv_counters(r, sl, self.num_kv_heads))
+
+        starts = range(0, t.shape[0], step)
+        if t.shape[0] > 64 * step:
+            # numpy releases the GIL inside these array operations: a few threads help
+            import concurrent.futures
+            with concurrent.futures.ThreadPoolExecutor(min(8, os.cpu_count() or 1)) as ex:
+                list(ex.map(rows, starts))
+        else:
+            for i in starts:
+                rows(i)
         plant = (self.plant_k if which == "k" else self.plant_v)[self.tok_base[r] + t]
         if plant.any():
             sel = plant.astype(bool)  # [len(t), Hkv]

@@ -61,6 +61,28 @@ class DeviceKV:
             sd.fill_cache(wl, "v", self.v, layout)
             self.block_table = layout.block_table
 
+    @classmethod
+    def from_rows(cls, wl: synth.Workload, rows_k: dict, rows_v: dict, device: str = "cuda"):
+        """Paged caches built on the host from per-request logical rows (uint16
+        [L, Hkv, 128] bf16 bits, e.g. regenerated with ``Workload.kv_rows``), so the
+        device holds exactly the bits the oracle is given."""
+        self = cls.__new__(cls)
+        self.wl = wl
+        shape = (wl.num_pages, wl.num_kv_heads, 16, 128)
+        self.block_table = torch.from_numpy(wl.block_table).to(device)
+        caches = []
+        for rows in (rows_k, rows_v):
+            cache = np.zeros(shape, dtype=np.uint16)
+            for r in range(wl.batch):
+                L = int(wl.seq_lens[r])
+                npg = (L + 15) // 16
+                pad = np.zeros((npg * 16, wl.num_kv_heads, 128), dtype=np.uint16)
+                pad[:L] = rows[r]
+                cache[wl.block_table[r, :npg]] = pad.reshape(npg, 16, wl.num_kv_heads, 128).transpose(0, 2, 1, 3)
+            caches.append(bf16_i16(cache).to(device))
+        self.k, self.v = caches
+        return self
+
     def kv(self):
         import sparse_self_speculative_gb300 as ss
         return ss.make_kv(self.k, self.v, self.block_table)
@@ -71,8 +93,13 @@ def zero_workspace(nbytes: int, device="cuda") -> torch.Tensor:
     return torch.zeros((nbytes + 7) // 8, dtype=torch.int64, device=device)
 
 
-def device_error(ws: torch.Tensor) -> int:
-    return int(ws.view(torch.int32)[0].item())
+def device_error(ws: torch.Tensor, clear: bool = False) -> int:
+    """The workspace's device error word, read through sspec_get_device_error on the
+    current stream (waits for the stream)."""
+    import sparse_self_speculative_gb300 as ss
+    out = torch.full((1,), -1, dtype=torch.int32, device=ws.device)
+    ss.sspec_get_device_error(ws, out, clear)
+    return int(out.item())
 
 
 class UnifiedStep:

@@ -144,9 +144,10 @@ def test_kv_offload_host_validation(lib):
     reaches CUDA (no GPU here)."""
     shape = ss.make_shape(16, 8)
     for fn in (lib.sspec_kv_offload, lib.sspec_kv_reload):
-        def call(shape=shape, k=4096, v=8192, num_pages=10, pages=16, n=3, hk=1 << 20, hv=2 << 20):
+        def call(shape=shape, k=4096, v=8192, num_pages=10, pages=16, n=3, hk=1 << 20, hv=2 << 20,
+                 host_bytes=3 * 8 * 16 * 128 * 2):
             return fn(ctypes.byref(shape) if shape is not None else None, k, v, num_pages, pages, n, hk, hv,
-                      None, None)
+                      host_bytes, None, None)
         assert call(shape=None) == ss.SSPEC_ERR_INVALID_ARG
         assert call(shape=ss.SspecShape(16, 8, 64, 16, 0.1)) == ss.SSPEC_ERR_UNSUPPORTED_SHAPE
         assert call(k=None) == ss.SSPEC_ERR_INVALID_ARG
@@ -158,7 +159,20 @@ def test_kv_offload_host_validation(lib):
         assert call(num_pages=0) == ss.SSPEC_ERR_INVALID_ARG
         assert call(k=4100) == ss.SSPEC_ERR_INVALID_ARG           # caches and host buffers 16-byte aligned
         assert call(hv=(2 << 20) + 8) == ss.SSPEC_ERR_INVALID_ARG
+        # host buffers shorter than the pages listed: rejected before the kernel could overrun them
+        assert call(host_bytes=3 * 8 * 16 * 128 * 2 - 1) == ss.SSPEC_ERR_INVALID_ARG
+        assert call(n=4) == ss.SSPEC_ERR_INVALID_ARG
         assert call(n=0, pages=None) == ss.SSPEC_OK               # empty list: nothing enqueued
+        assert call(n=0, pages=None, host_bytes=0) == ss.SSPEC_OK
+
+
+def test_device_error_accessor_host_validation(lib):
+    """sspec_get_device_error rejects null or misaligned pointers before enqueuing
+    anything (no GPU here, so only the rejections are exercised)."""
+    fn = lib.sspec_get_device_error
+    assert fn(None, 4096, 0, None) == ss.SSPEC_ERR_INVALID_ARG
+    assert fn(256, None, 0, None) == ss.SSPEC_ERR_INVALID_ARG
+    assert fn(264, 4096, 1, None) == ss.SSPEC_ERR_INVALID_ARG     # workspaces are 256-byte aligned
 
 
 def test_kv_fifo_matches_oracle_and_rejects_bad_arguments(lib):

@@ -114,7 +114,7 @@ def test_fifo_chunked_round_trip_keeps_attention_bit_identical():
             pages = dkv.block_table[r, first:first + count].contiguous()
             hk, hv = host[r]
             ss.sspec_kv_offload(shape, dkv.k, dkv.v, wl.num_pages, pages, count, hk.data_ptr() + first * page_bytes,
-                                hv.data_ptr() + first * page_bytes, err)
+                                hv.data_ptr() + first * page_bytes, err, host_bytes=(npg[r] - first) * page_bytes)
         torch.cuda.synchronize()
         old = {r: dkv.block_table[r, :npg[r]].clone() for r in (0, 2)}
         for r in (0, 2):                      # the pages are reused by someone else
@@ -128,7 +128,8 @@ def test_fifo_chunked_round_trip_keeps_attention_bit_identical():
             r, first, count = chunk
             hk, hv = host[r]
             ss.sspec_kv_reload(shape, dkv.k, dkv.v, wl.num_pages, new[r][first:first + count].contiguous(), count,
-                               hk.data_ptr() + first * page_bytes, hv.data_ptr() + first * page_bytes, err)
+                               hk.data_ptr() + first * page_bytes, hv.data_ptr() + first * page_bytes, err,
+                               host_bytes=(npg[r] - first) * page_bytes)
         for r in (0, 2):
             dkv.block_table[r, :npg[r]] = new[r]
         torch.cuda.synchronize()

@@ -2,7 +2,8 @@
 at sizes the oracle finishes in seconds that still span several tiles, chunks
 and ragged tails.
 
-Tolerances (stated by the problem, derived in the design doc for the rest):
+Tolerances (the attention and LSE bounds are the problem's own; the dump and
+average bounds follow from fp32 arithmetic over at most 64 rows):
   attention outputs   |gpu - oracle| <= 2e-2 + 1e-2 * |oracle|
   LSE                 |gpu - oracle| <= 1e-3
   dumped logits       |gpu - oracle| <= 1e-4 + 1e-5 * |oracle|   (-inf exactly where masked)
@@ -472,3 +473,30 @@ def test_fused_select_equals_separate_launches_bitwise(hq, hkv, s, long_lens):
         np.testing.assert_array_equal(st.d_idx.cpu().numpy(), ref["idx"])
         np.testing.assert_array_equal(st.d_nsel.cpu().numpy(), ref["nsel"])
         np.testing.assert_array_equal(S.cpu().numpy(), ref["S"])
+
+
+def test_device_error_accessor_reports_a_bad_page_and_clears():
+    """A block-table entry outside the page pool (planted on the host) is skipped by
+    the kernel and reported as SSPEC_DEVERR_PAGE_OOB through sspec_get_device_error,
+    into device memory and into page-locked host memory; clearing resets the word, and
+    the other request's outputs are bit-identical to a clean run's."""
+    import sparse_self_speculative_gb300 as ss
+    nq, hq, hkv = 8, 16, 8
+    wl = synth.make_workload("deverr", 606, hq, hkv, [300, 500])
+    dkv, q, loff, d, shape, ws = _verify_batch(wl, nq)
+    _run_verify(dkv, d, shape, ws, wl.batch, nq)
+    clean = hz.to_bits(d["out"]).copy()
+    bt = dkv.block_table.clone()
+    bt[1, 3] = wl.num_pages                       # one page of request 1 out of range
+    kv = ss.make_kv(dkv.k, dkv.v, bt)
+    ss.sspec_verify_attn(shape, kv, wl.batch, nq, d["q"], d["seq"], d["out"], d["lse"], d["logits"], d["loff"], ws)
+    dev_out = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    host_out = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    ss.sspec_get_device_error(ws, dev_out)
+    ss.sspec_get_device_error(ws, host_out, clear=True)
+    torch.cuda.synchronize()
+    assert int(dev_out.item()) == ss.SSPEC_DEVERR_PAGE_OOB
+    assert int(host_out.item()) == ss.SSPEC_DEVERR_PAGE_OOB
+    assert hz.device_error(ws) == 0                # cleared
+    np.testing.assert_array_equal(hz.to_bits(d["out"])[0], clean[0])
+    assert np.isfinite(oracle.bf16_bits_to_f64(hz.to_bits(d["out"])[1])).all()
