@@ -213,8 +213,11 @@ int sspec_sparse_draft_attn_noalloc(const sspec_shape* shape, const sspec_paged_
  * templates inside one persistent kernel; paper Sec. 4.2, Fig. 8 and Fig. 15).
  *
  * Request r verifies (as sspec_verify_attn with nq = k) when
- * bucket[r] == verify_bucket and otherwise takes one sparse draft step (as
- * sspec_sparse_draft_attn).  Query, output and LSE rows are ragged:
+ * bucket[r] == verify_bucket, sits the step out when bucket[r] < 0 (no work, its
+ * outputs untouched, nothing read but bucket[r]; a delayed-verification pipeline
+ * parks requests that wait for their verify results this way), and otherwise
+ * takes one sparse draft step (as sspec_sparse_draft_attn).  Query, output and
+ * LSE rows are ragged:
  *   q         device bf16 [rows][Hq][128]; request r owns rows q_off[r] ..
  *             q_off[r+1]-1 (k rows to verify, 1 row to draft)
  *   q_off     device int64 [batch+1]
@@ -271,6 +274,82 @@ int sspec_fused_step_select(const sspec_shape* shape, const sspec_paged_kv* kv, 
  *   bucket_out  host int32 [n_new]
  */
 int sspec_assign_buckets(int32_t k, int32_t* counts, int32_t n_new, int32_t* bucket_out);
+
+/*
+ * Delayed-verification pipeline: the host half
+ * (Delayed verification: the CPU work that turns a step's verify results into the
+ * next step's metadata leaves the critical path because only the requests that
+ * just verified -- 1/(k+1) of a unified batch -- wait one iteration, while every
+ * other request's metadata for the next step is prepared without the GPU's
+ * results; paper Sec. 4.3, Fig. 9).  Host only, not thread-safe; it allocates
+ * host memory at creation only.
+ *
+ * A request holds a slot r in [0, max_batch) from admission until it leaves:
+ * row r of the block table, of the pillar array (idx_off[r] .. idx_off[r+1],
+ * which must hold K of the longest length) and of every metadata array.
+ * Iteration t's verifying bucket is v_t = (-t) mod (k+1); a request of bucket b
+ * is at phase phi = (b - v_t) mod (k+1):
+ *   phi = 0   it verifies (nq = k rows, the last k tokens of its cache) if it is
+ *             new or has drafted since its last verification, else it drafts;
+ *   phi = 1   just verified: it sits out this iteration (the one-iteration delay:
+ *             the builder never waits for a verification's result);
+ *   else      it takes its next draft step, provided the result of its last
+ *             verification has been reported; otherwise it sits out (late).
+ * Lengths: a verification at cache length L selects pillars over [0, L); the
+ * caller then reports the length L' >= L the request continues from (acceptance
+ * belongs to the decoding loop); its draft step j attends over its pillars and
+ * [L, L' + j + 1), i.e. seq_len = L' + j + 1, sel_len = L, nsel = K(L).
+ *
+ *   sspec_pipeline_create   shape (heads), k, slots, sparsity s in (0,1] and the
+ *                           longest cache length a slot may reach (its block-table
+ *                           row); NULL for invalid arguments or no memory
+ *   sspec_pipeline_admit    a new request of cache length len (k <= len <= max_len)
+ *                           in a free slot; it joins the least-loaded bucket (ties
+ *                           to the lower id, as sspec_assign_buckets), returned in
+ *                           *bucket_out (nullable)
+ *   sspec_pipeline_leave    frees the slot; a result reported for it later is refused
+ *   sspec_pipeline_relabel  moves a request to another bucket (0..k), any time; a
+ *                           request waiting for its result keeps waiting
+ *   sspec_pipeline_report   the result of the verification the slot ran at
+ *                           `iteration`: the length it continues from
+ *                           (sel_len <= next_len < max_len); refused
+ *                           (SSPEC_ERR_INVALID_ARG) for any other iteration, a second
+ *                           report, or a free slot
+ *   sspec_pipeline_build    fills the host arrays of `meta` for `iteration`, which
+ *                           must be one more than the last built (every built step
+ *                           is assumed to run); counts go to *counts (nullable)
+ * The arrays are those of sspec_fused_step / sspec_fused_step_select for
+ * batch = max_batch and verify_bucket = 0 (bucket -1: sits out; 1.. : drafts).
+ * Build iteration t into one of two host buffer sets while iteration t-1's set is
+ * being copied and run; idx_off stays the caller's, constant per slot.
+ */
+typedef struct sspec_pipeline sspec_pipeline;
+typedef struct {
+  int32_t* bucket;      /* host [max_batch] */
+  int64_t* q_off;       /* host [max_batch + 1]: k rows to verify, 1 to draft, 0 to sit out */
+  int32_t* seq_lens;    /* host [max_batch] */
+  int32_t* sel_lens;    /* host [max_batch] */
+  int32_t* nsel;        /* host [max_batch]: pillar count of drafting requests, 0 otherwise */
+  int64_t* logit_off;   /* host [max_batch + 1]: Hkv * k * G * seq_len for verifying requests */
+} sspec_step_meta;
+typedef struct {
+  int32_t n_verify, n_draft;
+  int32_t n_waiting;    /* sitting out the one-iteration delay */
+  int32_t n_late;       /* sitting out because their result has not been reported */
+  int32_t n_blocked;    /* drafting would pass max_len */
+  int64_t rows;         /* query rows (q_off[max_batch]) */
+  int64_t logit_elems;  /* logit_off[max_batch] */
+  int64_t kv_tokens;    /* token count for sspec_workspace_size */
+} sspec_step_counts;
+sspec_pipeline* sspec_pipeline_create(const sspec_shape* shape, int32_t k, int32_t max_batch, float s,
+                                      int32_t max_len);
+void sspec_pipeline_destroy(sspec_pipeline* pipeline);
+int sspec_pipeline_admit(sspec_pipeline* pipeline, int32_t slot, int32_t len, int32_t* bucket_out);
+int sspec_pipeline_leave(sspec_pipeline* pipeline, int32_t slot);
+int sspec_pipeline_relabel(sspec_pipeline* pipeline, int32_t slot, int32_t bucket);
+int sspec_pipeline_report(sspec_pipeline* pipeline, int32_t slot, int64_t iteration, int32_t next_len);
+int sspec_pipeline_build(sspec_pipeline* pipeline, int64_t iteration, sspec_step_meta* meta,
+                         sspec_step_counts* counts);
 
 /*
  * KV-cache offload to host memory and reload

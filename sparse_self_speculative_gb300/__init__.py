@@ -44,6 +44,17 @@ class SspecPagedKV(ctypes.Structure):
                 ("num_pages", ctypes.c_int32)]
 
 
+class SspecStepMeta(ctypes.Structure):
+    _fields_ = [("bucket", ctypes.c_void_p), ("q_off", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("sel_lens", ctypes.c_void_p), ("nsel", ctypes.c_void_p), ("logit_off", ctypes.c_void_p)]
+
+
+class SspecStepCounts(ctypes.Structure):
+    _fields_ = [("n_verify", ctypes.c_int32), ("n_draft", ctypes.c_int32), ("n_waiting", ctypes.c_int32),
+                ("n_late", ctypes.c_int32), ("n_blocked", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("logit_elems", ctypes.c_int64), ("kv_tokens", ctypes.c_int64)]
+
+
 class SspecError(RuntimeError):
     def __init__(self, fn, code):
         super().__init__(f"{fn} returned {code}: {error_string(code)}")
@@ -76,6 +87,13 @@ _SIGS = {
     "sspec_kv_fifo_next": (ctypes.c_int, [_P, _I32, _P, _P, _P]),
     "sspec_kv_fifo_pending": (ctypes.c_int64, [_P]),
     "sspec_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "sspec_pipeline_create": (_P, [_P, _I32, _I32, ctypes.c_float, _I32]),
+    "sspec_pipeline_destroy": (None, [_P]),
+    "sspec_pipeline_admit": (ctypes.c_int, [_P, _I32, _I32, _P]),
+    "sspec_pipeline_leave": (ctypes.c_int, [_P, _I32]),
+    "sspec_pipeline_relabel": (ctypes.c_int, [_P, _I32, _I32]),
+    "sspec_pipeline_report": (ctypes.c_int, [_P, _I32, ctypes.c_int64, _I32]),
+    "sspec_pipeline_build": (ctypes.c_int, [_P, ctypes.c_int64, _P, _P]),
 }
 
 
@@ -262,6 +280,47 @@ def sspec_assign_buckets(k: int, counts, n_new: int):
     return list(out)[:n_new], list(c)
 
 
+def sspec_pipeline_create(shape: SspecShape, k: int, max_batch: int, s: float, max_len: int) -> int:
+    h = lib().sspec_pipeline_create(ctypes.byref(shape), k, max_batch, float(s), max_len)
+    if not h:
+        raise SspecError("sspec_pipeline_create", SSPEC_ERR_INVALID_ARG)
+    return h
+
+
+def sspec_pipeline_destroy(pipeline: int) -> None:
+    lib().sspec_pipeline_destroy(pipeline)
+
+
+def sspec_pipeline_admit(pipeline: int, slot: int, length: int) -> int:
+    """Admits a request into ``slot``; returns its bucket."""
+    b = ctypes.c_int32()
+    _check("sspec_pipeline_admit", lib().sspec_pipeline_admit(pipeline, slot, length, ctypes.byref(b)))
+    return b.value
+
+
+def sspec_pipeline_leave(pipeline: int, slot: int) -> None:
+    _check("sspec_pipeline_leave", lib().sspec_pipeline_leave(pipeline, slot))
+
+
+def sspec_pipeline_relabel(pipeline: int, slot: int, bucket: int) -> None:
+    _check("sspec_pipeline_relabel", lib().sspec_pipeline_relabel(pipeline, slot, bucket))
+
+
+def sspec_pipeline_report(pipeline: int, slot: int, iteration: int, next_len: int) -> None:
+    _check("sspec_pipeline_report", lib().sspec_pipeline_report(pipeline, slot, iteration, next_len))
+
+
+def sspec_pipeline_build(pipeline: int, iteration: int, meta: dict) -> SspecStepCounts:
+    """Fills the host arrays of ``meta`` (keys bucket, q_off, seq_lens, sel_lens, nsel,
+    logit_off: contiguous int32 / int64 CPU tensors or numpy arrays) for ``iteration``."""
+    def addr(a):
+        return a.ctypes.data if hasattr(a, "ctypes") else a.data_ptr()
+    m = SspecStepMeta(*(addr(meta[n]) for n in ("bucket", "q_off", "seq_lens", "sel_lens", "nsel", "logit_off")))
+    c = SspecStepCounts()
+    _check("sspec_pipeline_build", lib().sspec_pipeline_build(pipeline, iteration, ctypes.byref(m), ctypes.byref(c)))
+    return c
+
+
 def _nbytes(t):
     if t is None:
         return 0
@@ -274,4 +333,6 @@ __all__ = [
     "sspec_fused_step", "sspec_fused_step_select", "sspec_sparse_draft_attn_noalloc", "sspec_assign_buckets",
     "sspec_kv_offload", "sspec_kv_reload", "sspec_kv_fifo_create", "sspec_kv_fifo_destroy", "sspec_kv_fifo_push",
     "sspec_kv_fifo_next", "sspec_kv_fifo_pending", "sspec_get_device_error", "header_functions",
+    "SspecStepMeta", "SspecStepCounts", "sspec_pipeline_create", "sspec_pipeline_destroy", "sspec_pipeline_admit",
+    "sspec_pipeline_leave", "sspec_pipeline_relabel", "sspec_pipeline_report", "sspec_pipeline_build",
 ]

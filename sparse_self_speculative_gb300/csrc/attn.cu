@@ -56,6 +56,8 @@ __device__ __forceinline__ bool is_verify(const AttnParams& p, int r) {
 // Reads request r's description; returns false (and reports, when asked) if its
 // lengths are inconsistent, in which case the request is skipped.
 __device__ bool load_req(const AttnParams& p, int r, Req& q, bool report) {
+  // a negative bucket: the request sits this step out (no work, nothing reported)
+  if (p.mode == kByBucket && p.bucket[r] < 0) return false;
   q.verify = is_verify(p, r);
   q.L = p.seq_lens[r];
   const int cap = p.max_pages * kPage;
