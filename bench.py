@@ -522,7 +522,98 @@ def kv_offload_context(st, n_pages: int = 4096, reps: int = 5):
     }
 
 
-def cpu_baseline(st, seconds: float = 15.0, n_verify: int = 2, n_draft: int = 16):
+class HostStep:
+    """Host copies of one step's inputs for the C oracle of a whole step: the paged
+    caches (bf16 bits, read back from the seeded device fill), the block table, the
+    queries, lengths and the drafting requests' pillars."""
+
+    def __init__(self, st):
+        from tests import harness as hz
+        self.st = st
+        self.k = hz.to_bits(st.dkv.k)
+        self.v = hz.to_bits(st.dkv.v)
+        self.idx = st.d_idx.cpu().numpy()
+
+    @staticmethod
+    def fits(st, margin: float = 2.5) -> bool:
+        try:
+            avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+        except (ValueError, OSError):
+            return True
+        need = 2 * st.dkv.k.numel() * 2
+        return avail > margin * need + (8 << 30)
+
+    def args(self, reqs):
+        """pillar_step's request arrays for the requests `reqs` (batch order)."""
+        st, wl = self.st, self.st.wl
+        reqs = np.asarray(reqs, dtype=np.int64)
+        rows = st.q_off[reqs + 1] - st.q_off[reqs]
+        q_off = np.zeros(len(reqs) + 1, dtype=np.int64)
+        q_off[1:] = np.cumsum(rows)
+        q = np.concatenate([st.q_bits[st.q_off[r]:st.q_off[r + 1]] for r in reqs])
+        blocks = [self.idx[st.idx_off[r]:st.idx_off[r + 1]] if not st.is_verify[r] else self.idx[:0] for r in reqs]
+        idx_off = np.zeros(len(reqs) + 1, dtype=np.int64)
+        idx_off[1:] = np.cumsum([len(b) for b in blocks])
+        idx = np.concatenate(blocks + [np.zeros(1, dtype=np.int32)])
+        return dict(block_table=wl.block_table[reqs], seq_lens=wl.seq_lens[reqs],
+                    verify=st.is_verify[reqs].astype(np.int32), q_off=q_off, q=q, sel_lens=st.sel_lens[reqs],
+                    idx=idx, idx_off=idx_off, nsel=st.nsel_host[reqs])
+
+    def run(self, reqs, threads: int) -> float:
+        """Seconds for one step of the C oracle over `reqs`."""
+        from oracle import c_step
+        from tests import harness as hz
+        a = self.args(reqs)
+        st = self.st
+        t0 = time.perf_counter()
+        c_step.pillar_step(self.k, self.v, a["block_table"], a["seq_lens"], a["verify"], a["q_off"], a["q"],
+                           a["sel_lens"], a["idx"], a["idx_off"], a["nsel"], st.wl.num_q_heads, st.k, hz.SCALE, st.s,
+                           threads)
+        return time.perf_counter() - t0
+
+    def tokens(self, reqs) -> int:
+        v = self.st.is_verify[np.asarray(reqs)]
+        return int(self.st.k * v.sum() + (~v).sum())
+
+
+def _sample_requests(st, frac: float):
+    """The first ceil(frac * n) verifying and drafting requests in batch order."""
+    vr, dr = np.flatnonzero(st.is_verify), np.flatnonzero(~st.is_verify)
+    nv = min(len(vr), max(1, int(math.ceil(frac * len(vr)))))
+    nd = min(len(dr), max(1, int(math.ceil(frac * len(dr)))))
+    return np.sort(np.concatenate([vr[:nv], dr[:nd]])), nv, nd
+
+
+def cpu_baseline(st, seconds: float = 8.0):
+    """The C oracle of a whole step (oracle/c/pillar_step.c: the numpy oracle's
+    definitions as plain double-precision loops, one thread per host core over
+    (request, KV head) jobs) timed on the host cores over the whole benchmark step,
+    with the pillars the device step uses; one thread on a bounded sample beside it."""
+    if not HostStep.fits(st):
+        return dict(numpy_sample_baseline(st), note="host memory too small for the whole step's caches")
+    hs = HostStep(st)
+    B = st.wl.batch
+    allr = np.arange(B)
+    cores = os.cpu_count() or 1
+    hs.run(allr, cores)                                # warm-up (page faults of the host copies)
+    dts = []
+    while sum(dts) < seconds or not dts:
+        dts.append(hs.run(allr, cores))
+        if len(dts) >= 5:
+            break
+    dt = statistics.median(dts)
+    nv, nd = int(st.is_verify.sum()), int((~st.is_verify).sum())
+    one_r, one_v, one_d = _sample_requests(st, 0.125)
+    t1 = hs.run(one_r, 1)
+    return {"value": hs.tokens(allr) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the whole step: {nv} verify + {nd} draft requests, median of {len(dts)} steps "
+                      f"({dt:.2f} s each; C oracle, double precision, {cores} threads)",
+            "one_thread": {"value": hs.tokens(one_r) / t1, "unit": UNIT, "cores": 1,
+                           "sample": f"{one_v} verify + {one_d} draft requests of the step, one step "
+                                     f"({t1:.2f} s; C oracle, 1 thread)"}}
+
+
+def numpy_sample_baseline(st, seconds: float = 15.0, n_verify: int = 2, n_draft: int = 16):
     """The oracle as it stands, timed on the host cores over a bounded sample of the
     same step (the first verifying and drafting requests in batch order, with the
     pillars the device step uses), repeated until about `seconds` of oracle time."""
@@ -566,25 +657,7 @@ def cpu_baseline(st, seconds: float = 15.0, n_verify: int = 2, n_draft: int = 16
         passes += 1
     return {"value": tokens * passes / t, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{len(v_ids)} verify + {len(d_ids)} draft requests of the step, "
-                      f"{passes} passes in {t:.1f} s (numpy float64 oracle)",
-            "one_thread": oracle_one_thread()}
-
-
-def oracle_one_thread(steps: int = 3):
-    """The reference arm's oracle sample timed again in a child process whose BLAS and
-    OpenMP pools hold one thread (set before numpy loads): the 1-thread baseline."""
-    env = {k: v for k, v in os.environ.items()
-           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
-        env[var] = "1"
-    try:
-        out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps",
-                              str(steps), "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
-        line = json.loads(out.stdout.strip().splitlines()[-1])
-        return {"value": line["value"], "unit": line["unit"], "cores": 1,
-                "sample": line["cpu_baseline"]["sample"] + f", {steps} timed steps"}
-    except Exception as e:   # the baseline is context: report why it is missing
-        return {"value": None, "unavailable": f"{type(e).__name__}: {e}"[:200]}
+                      f"{passes} passes in {t:.1f} s (numpy float64 oracle)"}
 
 
 def _blas_threads():
@@ -600,6 +673,63 @@ def _blas_threads():
 # reference arm: the CPU oracle on the host cores
 # --------------------------------------------------------------------------------------
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores, on this arm's
+    workload.  With a GPU on the box, the seeded device fill writes the caches (input
+    generation only: no kernel of the library runs) and the C oracle of a whole step
+    times the step itself, or, when --steps is large, an equal share of its verifying
+    and drafting requests per step so that the run stays within a few minutes.  Without
+    one, the numpy oracle times a sample of requests regenerated on the host."""
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:
+        has_gpu = False
+    if not has_gpu:
+        return _reference_numpy(args)
+    import synth
+    import sparse_self_speculative_gb300 as ss
+    from tests import harness as hz
+
+    torch.cuda.set_device(0)
+    name = args.workload
+    hq, hkv, B, k, s = synth.WORKLOADS[name]
+    seed = 1000 * 3
+    lens = synth.workload_lengths(name, seed)
+    if args.batch:
+        lens = lens[:args.batch]
+        B = len(lens)
+    wl = synth.named_workload(name, seed, seq_lens=lens)
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
+    dkv = hz.DeviceKV(wl, fill="device")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="synthetic")
+    torch.cuda.synchronize()
+    if not HostStep.fits(st):
+        return _reference_numpy(args)
+    hs = HostStep(st)
+    cores = os.cpu_count() or 1
+    t_full = hs.run(np.arange(B), cores)              # also the first warm-up
+    budget_s = 150.0
+    frac = min(1.0, budget_s / max(1e-9, (args.steps + args.warmup) * t_full))
+    reqs, nv, nd = _sample_requests(st, frac)
+    for _ in range(max(0, args.warmup - 1)):
+        hs.run(reqs, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        hs.run(reqs, cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = hs.tokens(reqs) / dt
+    what = "the whole step" if frac >= 1.0 else "a share of the step"
+    sample = (f"{what}: {nv} verify + {nd} draft requests of {int(st.is_verify.sum())} + "
+              f"{int((~st.is_verify).sum())} (C oracle, double precision, {cores} threads)")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": name, "global_batch": B, "parallelism": "cpu"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _reference_numpy(args):
     import oracle
     import synth
     from tests import harness as hz
@@ -648,7 +778,7 @@ def run_reference(args):
     tokens = k * len(v_ids) + len(d_ids)
     value = tokens / dt
     cores = _blas_threads()
-    sample = f"{len(v_ids)} verify + {len(d_ids)} draft requests of the step (numpy float64 oracle)"
+    sample = f"{len(v_ids)} verify + {len(d_ids)} draft requests of the step (numpy float64 oracle; no GPU for the input fill)"
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
