@@ -55,9 +55,14 @@ __device__ __forceinline__ bool is_verify(const AttnParams& p, int r) {
 
 // Reads request r's description; returns false (and reports, when asked) if its
 // lengths are inconsistent, in which case the request is skipped.
+// A request whose bucket is negative sits the step out: the scans that enumerate
+// requests give it no units (the check stays out of load_req, which the per-unit path
+// inlines).
+__device__ __forceinline__ bool sits_out(const AttnParams& p, int r) {
+  return p.mode == kByBucket && p.bucket[r] < 0;
+}
+
 __device__ bool load_req(const AttnParams& p, int r, Req& q, bool report) {
-  // a negative bucket: the request sits this step out (no work, nothing reported)
-  if (p.mode == kByBucket && p.bucket[r] < 0) return false;
   q.verify = is_verify(p, r);
   q.L = p.seq_lens[r];
   const int cap = p.max_pages * kPage;
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       const int r = tid * per + i;
       rT[i] = rL[i] = rflags[i] = 0;
       Req q;
-      if (i < per && r < B && load_req(p, r, q, blockIdx.x == 0)) {
+      if (i < per && r < B && !sits_out(p, r) && load_req(p, r, q, blockIdx.x == 0)) {
         int K;
         const bool sel = p.sel_scores != nullptr && q.verify && sel_request_ok(p, r, q, &K, blockIdx.x == 0);
         rT[i] = q.T;
@@ -458,11 +463,11 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     }
     block_exclusive_scan<kThreads>(uf, s_warp, &tf);
     block_exclusive_scan<kThreads>(a1, s_warp, &ta);
-    const int want = 3 * int(gridDim.x) / 2;
+    const int want = 3 * p.grid_full / 2;
     vchunk = t4 + td >= want ? 4 * kChunk : (t2 + td >= want ? 2 * kChunk : kChunk);
     n_draft = td;
     n_full = tf;
-    avg_passes = min(avg_max_passes(kThreads), max(1, ta / int(gridDim.x)));
+    avg_passes = min(avg_max_passes(kThreads), max(1, ta / p.grid_full));
     const int blk = kThreads * kAvgPass * avg_passes;
     int sum = 0, an = 0;
 #pragma unroll
@@ -505,7 +510,8 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       if (r < B) {
         Req q;
         int units = 0;
-        if (load_req(p, r, q, false) && !q.verify) units = ((q.T + kChunk - 1) / kChunk - 1) * p.hkv;
+        if (!sits_out(p, r) && load_req(p, r, q, false) && !q.verify)
+          units = ((q.T + kChunk - 1) / kChunk - 1) * p.hkv;
         s_prefix[r + 1] = units;
         sum += units;
       }
@@ -524,7 +530,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   };
   auto last_band = [&](int r) -> int {   // -1: not a valid draft request
     Req q;
-    if (!load_req(p, r, q, false) || q.verify) return -1;
+    if (sits_out(p, r) || !load_req(p, r, q, false) || q.verify) return -1;
     const int last = q.T - ((q.T + kChunk - 1) / kChunk - 1) * kChunk;
     const int tiles = (last + kTile - 1) / kTile;
     return tiles > 9 ? 0 : (tiles > 6 ? 1 : (tiles > 3 ? 2 : 3));
@@ -1015,8 +1021,17 @@ cudaError_t launch_mt(const AttnParams& p, cudaStream_t stream) {
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_persistent<MT, WN>, W * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int grid = device_sm_count() * per_sm;
-  attn_persistent<MT, WN><<<grid, W * 32, smem, stream>>>(p);
+  // Every CTA of the persistent grid takes tasks until none is left, so a small batch
+  // needs no more CTAs than it can have tasks: attention units of at least kChunk
+  // entries and averaging items of at least kAvgPass positions per thread, over every
+  // (request, kv head), for sequences as long as the block-table row allows.
+  AttnParams q = p;
+  q.grid_full = device_sm_count() * per_sm;
+  const long long per_head = (16LL * p.max_pages + kChunk - 1) / kChunk +
+                             (p.sel_scores ? (16LL * p.max_pages + W * 32 * kAvgPass - 1) / (W * 32 * kAvgPass) : 0);
+  const long long tasks = (long long)p.batch * p.hkv * per_head;
+  const int grid = int(tasks < q.grid_full ? (tasks > 0 ? tasks : 1) : q.grid_full);
+  attn_persistent<MT, WN><<<grid, W * 32, smem, stream>>>(q);
   return cudaGetLastError();
 }
 

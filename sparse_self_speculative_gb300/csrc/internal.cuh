@@ -129,6 +129,9 @@ struct AttnParams {
   float* partials;
   long long unit_capacity;
   int rows_max;               // rows of a partial state
+  int grid_full;              // CTAs the device holds at once (set by the launcher); the unit
+                              // and averaging-item sizes are chosen for this many CTAs, so a
+                              // launch with fewer CTAs computes the same bits
   long long unit_stride;      // floats between consecutive partial states
   int32_t* draft_base;        // [batch]: first partial-state slot of each request's draft units
   // pillar selection of the verifying requests inside the same launch (sel_scores null: off)

@@ -240,3 +240,30 @@ def test_reference_arm_json_line_has_the_contract_keys():
     assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+
+
+def test_attention_templates_do_not_spill():
+    """The attention templates stay within their register budgets (a spill in the
+    per-tile loop costs several percent on the GB300: one was caught this way).  Compiled
+    here for sm_103a with ptxas's resource report; the 64-row template, which no
+    benchmark workload uses, is allowed its few spilled bytes."""
+    import re
+    import subprocess
+    from sparse_self_speculative_gb300 import _build
+    src = os.path.join(_build.CSRC, "attn.cu")
+    res = subprocess.run([_build.nvcc()] + _build._flags(["-Xptxas", "-v"]) + ["-c", src, "-o", os.devnull],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr[-2000:]
+    report = {}
+    current = None
+    for line in res.stderr.splitlines():
+        m = re.search(r"Compiling entry function '.*attn_persistentILi(\d)ELi(\d)E", line)
+        if m:
+            current = (int(m.group(1)), int(m.group(2)))
+        m = re.search(r"(\d+) bytes spill stores", line)
+        if m and current is not None:
+            report[current] = int(m.group(1))
+            current = None
+    assert set(report) == {(1, 4), (2, 4), (3, 2), (4, 2)}, report
+    for key, spill in report.items():
+        assert spill == 0 or key == (4, 2), (key, spill)
