@@ -266,16 +266,40 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     assert hz.device_error(st.ws) == 0, "device error word set"
 
-    # ---- device-resident timed region ----
-    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_s1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # ---- device-resident timed region: the K steps, captured once as a CUDA graph and
+    # replayed back to back (a serving loop captures its step the same way); CUDA events
+    # only around the replay, so the average step is the kernel's own time between
+    # neighbours.  Stream-launched steps with an event pair around each launch are timed
+    # after it as context (their per-step distribution and the launch overhead). ----
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            step()
+    graph.replay()                       # first replay of the captured graph, untimed
+    torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     clk_lo = clk.mark()
     start.record(stream)
-    for i in range(args.steps):
+    graph.replay()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk_hi = clk.mark()
+    barrier(world)
+    assert hz.device_error(st.ws) == 0, "device error word set"
+    total_ms = start.elapsed_time(stop)
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+    tokens_all = sum_over_ranks(acc["query_tokens"] * args.steps, world)
+    value = tokens_all / (ms_step * args.steps / 1e3)
+    del graph
+
+    # ---- context: stream-launched steps, an event pair around each launch ----
+    n_ctx = min(args.steps, 50)
+    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ctx)]
+    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ctx)]
+    ev_s1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_ctx)]
+    for i in range(n_ctx):
         ev_f0[i].record(stream)
         if fused_sel:
             st.fused_select(S)
@@ -285,18 +309,10 @@ def run_ours(args, world, rank, local):
             ev_f1[i].record(stream)
             st.select(avg_scores=S)
         ev_s1[i].record(stream)
-    stop.record(stream)
     torch.cuda.synchronize()
-    clk_hi = clk.mark()
     clk.__exit__()
-    barrier(world)
-    assert hz.device_error(st.ws) == 0, "device error word set"
-    total_ms = start.elapsed_time(stop)
     fused_ms = [a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)]
     select_ms = [a.elapsed_time(b) for a, b in zip(ev_f1, ev_s1)]
-    ms_step = max_over_ranks(total_ms / args.steps, world)
-    tokens_all = sum_over_ranks(acc["query_tokens"] * args.steps, world)
-    value = tokens_all / (ms_step * args.steps / 1e3)
 
     # ---- end to end: host buffers in, results out, every step ----
     # As a serving loop runs it: two sets of per-step device buffers, host-to-device
@@ -395,7 +411,9 @@ def run_ours(args, world, rank, local):
     attn_only_ms = o0.elapsed_time(o1) / n_other
 
     peak, peak_kind = _peaks()
-    f_ms = statistics.mean(fused_ms)
+    # the dominant launch's average duration: the graph-replayed steps when the step is
+    # that one launch; the stream-launched measurement when the selection has its own
+    f_ms = ms_step if fused_sel else statistics.mean(fused_ms)
     # the dominant kernel: the fused launch (with the selection when it runs inside it).
     # Its algorithmic bytes are the K and V bytes (every row once); the bytes of the
     # dump, the selection, queries, outputs and indices are reported beside them.
@@ -405,7 +423,7 @@ def run_ours(args, world, rank, local):
     traffic = None if ratio is None else kbytes * ratio
     kv_gbs = acc["kv_bytes"] / (f_ms / 1e3) / 1e9
     total_gbs = acc["fused_bytes"] / (f_ms / 1e3) / 1e9
-    gpu_launches = (1 if fused_sel else 2) * args.steps
+    gpu_launches = (1 if fused_sel else 2) * args.steps   # inside the timed graph replay
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -418,8 +436,11 @@ def run_ours(args, world, rank, local):
         "kv_gbs": kv_gbs,
         "selection": "inside the fused launch" if fused_sel else "separate launch",
         "fused_ms": f_ms, "select_ms": None if fused_sel else statistics.mean(select_ms),
-        "step_ms": dict(_dist([a.elapsed_time(b) for a, b in zip(ev_f0, ev_s1)]),
-                        what="per-step device time, event before the step's first launch to after its last"),
+        "timing": f"{args.steps} steps captured in one CUDA graph, replayed back to back; events around the replay",
+        "stream_launched": {"ms_per_launch_mean": statistics.mean(fused_ms), "n": n_ctx,
+                            "step_ms": dict(_dist([a.elapsed_time(b) for a, b in zip(ev_f0, ev_s1)]),
+                                            what="per-step device time with an event pair around each "
+                                                 "stream-launched step")},
         f"ms_per_step_{other}_selection": other_ms,
         "roofline": {"bound": "hbm", "achieved": kv_gbs, "peak": peak, "unit": "GB/s", "frac": kv_gbs / peak,
                      "traffic": traffic,
