@@ -107,9 +107,9 @@ def test_single_request_cycle_2k():
 
 def _rows_from_cache(dkv, r, positions):
     """K and V rows (float64, [n, Hkv, 128]) of request r at `positions`, read back from
-    the device caches the input generator filled (the attention path never writes them;
-    the device generator's bits equal the host generator's, which is tested).  At these
-    lengths regenerating the rows on the host would take minutes."""
+    the device caches the input generator filled (the attention path never writes them).
+    The device generator's bits equal the host generator's: tested on small requests and,
+    in each workload below, on its longest verifying request in full."""
     pos = torch.as_tensor(np.asarray(positions, dtype=np.int64), device="cuda")
     pages = dkv.block_table[r].long()[pos // 16]
     slots = pos % 16
@@ -159,6 +159,14 @@ def test_unified_step_full_size(name):
         for h in range(hkv):
             got = idx[st.idx_off[r] + h * stride: st.idx_off[r] + h * stride + K]
             assert np.all(np.diff(got) > 0) and got[0] >= 0 and got[-1] < L[r]
+    # the rows the oracle reads come from the device caches; at this size, the longest
+    # verifying request's rows regenerated on the host must equal them bit for bit
+    rl = int(vr[np.argmax(L[vr])])
+    for which, cache in (("k", dkv.k), ("v", dkv.v)):
+        pos = np.arange(int(L[rl]))
+        dev = hz.to_bits(cache[dkv.block_table[rl].long()[torch.from_numpy(pos // 16).cuda()], :,
+                               torch.from_numpy(pos % 16).cuda(), :])
+        np.testing.assert_array_equal(dev, wl.kv_rows(which, rl, pos))
     # element-wise parity: every verifying request and a seeded sample of 16 drafts
     rng = np.random.default_rng(7)
     sample_v = vr
