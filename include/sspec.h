@@ -75,6 +75,9 @@ enum {
 #define SSPEC_MAX_BATCH 1024
 /* Largest number of query rows per (request, KV head): nq * G for verification. */
 #define SSPEC_MAX_ROWS 64
+/* Longest token list of one request: seq_len to verify, nsel + seq_len - sel_len for a
+   draft step.  A longer request is skipped and reported with SSPEC_DEVERR_LENGTH. */
+#define SSPEC_MAX_TOKENS 196608
 
 typedef struct {
   int32_t num_q_heads;   /* Hq */

@@ -30,6 +30,7 @@ SSPEC_DEVERR_WORKSPACE = 16
 SSPEC_DEVERR_TIMEOUT = 32
 SSPEC_MAX_BATCH = 1024
 SSPEC_MAX_ROWS = 64
+SSPEC_MAX_TOKENS = 196608
 
 
 class SspecShape(ctypes.Structure):

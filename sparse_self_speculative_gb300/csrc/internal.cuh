@@ -24,6 +24,7 @@ constexpr int kMaxChunks = 256;    // per (request, kv head): bounds the merge s
 constexpr int kTile = 64;          // tokens per pipeline stage
 constexpr int kStages = 2;         // cp.async pipeline depth (two CTAs per SM for every shape)
 static_assert(kChunk % kTile == 0 && kVerifyChunkMax / kPage <= kChunk, "verification unit row ids fit");
+static_assert(kMaxChunks * kChunk == SSPEC_MAX_TOKENS, "the documented token limit");
 
 // ---- selection work decomposition ----------------------------------------------------
 constexpr int kSelBlock = 4096;    // tokens averaged per unit

@@ -52,7 +52,7 @@ __device__ bool load_sel_req(const SelectParams& p, int r, SelReq& q, bool repor
   q.ibase = p.idx_off[r];
   q.istride = (p.idx_off[r + 1] - p.idx_off[r]) / p.hkv;
   q.K = sel::pillar_count(p.s, q.L);
-  if (q.L < p.nq) bad |= SSPEC_DEVERR_LENGTH;
+  if (q.L < p.nq || q.L > SSPEC_MAX_TOKENS) bad |= SSPEC_DEVERR_LENGTH;
   if (p.q_off && p.q_off[r + 1] - p.q_off[r] < p.nq) bad |= SSPEC_DEVERR_LENGTH;
   if (range < (long long)p.hkv * q.rows * q.L || q.loff % q.rows != 0 || q.istride < q.K)
     bad |= SSPEC_DEVERR_RANGE;

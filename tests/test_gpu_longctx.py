@@ -223,3 +223,64 @@ def test_fused_step_select_64k_128k(setup, k):
                                                  hz.SCALE)
     hz.check_close_bf16(out_b[q_off[2]], o_ref, OUT_ATOL, OUT_RTOL)
     assert np.abs(lse_h[q_off[2]] - l_ref).max() <= LSE_TOL
+
+
+def test_longest_request_and_one_token_beyond():
+    """A request at SSPEC_MAX_TOKENS (196,608 tokens, 64 chunks of 3,072 or 256 of 768)
+    verifies and selects like any other (every row regenerated on the host for the
+    oracle); a request one token longer in the same launch is skipped and reported with
+    SSPEC_DEVERR_LENGTH, its outputs, dump and pillar count left as they were."""
+    import sparse_self_speculative_gb300 as ss
+    torch.cuda.set_device(0)
+    nq = 8
+    Lmax = ss.SSPEC_MAX_TOKENS
+    lens = [Lmax, Lmax + 1]
+    wl = synth.make_workload("maxlen", 6006, HQ, HKV, lens)
+    dkv = hz.DeviceKV(wl, fill="device")
+    shape = ss.make_shape(HQ, HKV)
+    B = 2
+    L = np.array(lens, dtype=np.int64)
+    q = np.stack([wl.q_rows(r, np.arange(nq)) for r in range(B)])
+    loff = np.zeros(B + 1, dtype=np.int64)
+    loff[1:] = np.cumsum(HKV * nq * G * L)
+    K = np.array([oracle.pillar_count(S, int(x)) for x in L], dtype=np.int64)
+    ioff = np.zeros(B + 1, dtype=np.int64)
+    ioff[1:] = np.cumsum(HKV * K)
+    d_seq = torch.from_numpy(L.astype(np.int32)).cuda()
+    out = torch.full((B, nq, HQ, 128), 0x7FC0, dtype=torch.int16, device="cuda")   # bf16 NaN sentinels
+    lse = torch.full((B, nq, HQ), 7.0, dtype=torch.float32, device="cuda")
+    logits = torch.full((int(loff[-1]),), 3.0, dtype=torch.float32, device="cuda")
+    d_loff = torch.from_numpy(loff).cuda()
+    Sd = torch.zeros(int(HKV * L.sum()), dtype=torch.float32, device="cuda")
+    idx = torch.full((int(ioff[-1]),), -1, dtype=torch.int32, device="cuda")
+    nsel = torch.full((B,), -5, dtype=torch.int32, device="cuda")
+    ws = hz.zero_workspace(ss.sspec_workspace_size(shape, B, nq, int(L.sum())))
+    ss.sspec_verify_attn(shape, dkv.kv(), B, nq, hz.bf16_i16(q).cuda(), d_seq, out, lse, logits, d_loff, ws)
+    ss.sspec_select_pillars(shape, B, nq, S, logits, d_loff, lse, None, d_seq, Sd, idx, torch.from_numpy(ioff).cuda(),
+                            nsel, ws)
+    torch.cuda.synchronize()
+    assert hz.device_error(ws) == ss.SSPEC_DEVERR_LENGTH
+    out_b, lse_h, lg_h = hz.to_bits(out), lse.cpu().numpy(), logits.cpu().numpy()
+    nsel_h, idx_h, S_h = nsel.cpu().numpy(), idx.cpu().numpy(), Sd.cpu().numpy()
+    # the request one token too long: untouched
+    assert (out_b[1] == 0x7FC0).all() and (lse_h[1] == 7.0).all() and (lg_h[loff[1]:] == 3.0).all()
+    assert nsel_h[1] == -5 and (idx_h[ioff[1]:] == -1).all()
+    # the longest request: against the oracle on host-regenerated rows
+    kf = oracle.bf16_bits_to_f64(wl.kv_rows("k", 0, np.arange(Lmax)))
+    vf = oracle.bf16_bits_to_f64(wl.kv_rows("v", 0, np.arange(Lmax)))
+    o_ref, l_ref, lg_ref = oracle.verify_attention(oracle.bf16_bits_to_f64(q[0]), kf, vf, hz.SCALE)
+    del kf, vf
+    hz.check_close_bf16(out_b[0], o_ref, OUT_ATOL, OUT_RTOL)
+    assert np.abs(lse_h[0] - l_ref).max() <= LSE_TOL
+    lg = lg_h[:loff[1]].reshape(HKV, nq * G, Lmax)
+    masked = np.isneginf(lg_ref)
+    np.testing.assert_array_equal(np.isneginf(lg), masked)
+    assert np.all(np.abs(lg[~masked] - lg_ref[~masked]) <= 1e-4 + 1e-5 * np.abs(lg_ref[~masked]))
+    S_ref = oracle.average_scores(lg_ref, l_ref, G)
+    Sg = S_h[: HKV * Lmax].reshape(HKV, Lmax).astype(np.float64)
+    assert np.all(np.abs(Sg - S_ref) <= 1e-4 * S_ref + 1e-9)
+    assert nsel_h[0] == K[0]
+    for h in range(HKV):
+        np.testing.assert_array_equal(idx_h[h * K[0]:(h + 1) * K[0]], oracle.top_k_pillars(Sg[h], int(K[0])))
+    del dkv
+    torch.cuda.empty_cache()

@@ -500,3 +500,45 @@ def test_device_error_accessor_reports_a_bad_page_and_clears():
     assert hz.device_error(ws) == 0                # cleared
     np.testing.assert_array_equal(hz.to_bits(d["out"])[0], clean[0])
     assert np.isfinite(oracle.bf16_bits_to_f64(hz.to_bits(d["out"])[1])).all()
+
+
+def test_fused_step_select_at_the_maximum_batch():
+    """SSPEC_MAX_BATCH (1,024) requests of 16 to 300 tokens in one fused launch with the
+    selection inside: every request against the oracle, every verifying request's
+    pillars against the oracle's Top-K of the GPU's averages."""
+    import sparse_self_speculative_gb300 as ss
+    k, s, hq, hkv = 8, 0.05, 16, 8
+    G = hq // hkv
+    B = ss.SSPEC_MAX_BATCH
+    lens = np.random.default_rng(11).integers(16, 300, size=B).astype(np.int32)
+    wl = synth.make_workload("maxbatch", 1024, hq, hkv, lens, plant="kv_per_head", plant_frac=0.03)
+    buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
+    dkv = hz.DeviceKV(wl, fill="host")
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, pillars="synthetic")
+    S_all = st.score_buffer()
+    st.fused_select(S_all)
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0
+    out, lse = hz.to_bits(st.d_out), st.d_lse.cpu().numpy()
+    S_np, idx = S_all.cpu().numpy(), st.d_idx.cpu().numpy()
+    for r in range(B):
+        L = int(wl.seq_lens[r])
+        rows = slice(st.q_off[r], st.q_off[r + 1])
+        kf, vf = st.kv_f64(r, np.arange(L))
+        if st.is_verify[r]:
+            o_ref, l_ref, lg_ref = oracle.verify_attention(st.q_f64(r), kf, vf, hz.SCALE)
+            S_ref = oracle.average_scores(lg_ref, l_ref, G)
+            soff = st.logit_off[r] // (k * G)
+            Sg = S_np[soff: soff + hkv * L].reshape(hkv, L).astype(np.float64)
+            assert np.all(np.abs(Sg - S_ref) <= 1e-4 * S_ref + 1e-9)
+            K = oracle.pillar_count(s, L)
+            stride = (st.idx_off[r + 1] - st.idx_off[r]) // hkv
+            for h in range(hkv):
+                got = idx[st.idx_off[r] + h * stride: st.idx_off[r] + h * stride + K]
+                np.testing.assert_array_equal(got, oracle.top_k_pillars(Sg[h], K))
+        else:
+            o_ref, l_ref = oracle.sparse_draft_attention(st.q_f64(r)[0], kf, vf, st.pillars[r], int(st.sel_lens[r]),
+                                                         hz.SCALE)
+            o_ref, l_ref = o_ref[None], l_ref[None]
+        hz.check_close_bf16(out[rows], o_ref, OUT_ATOL, OUT_RTOL)
+        assert np.abs(lse[rows] - l_ref).max() <= LSE_TOL
