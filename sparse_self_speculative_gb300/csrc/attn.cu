@@ -204,10 +204,10 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
 // When the last chunk of a verifying (request, kv head) completes (its output and LSE
 // are final), that CTA publishes the head's averaging items on a second queue: slots
 // are reserved with an atomic counter and then filled with (request, head, block)
-// descriptors.  CTAs take published averaging items before attention units, so the
-// head's logit dump is read back soon after it was written.  The last averaging item
-// of a head to finish runs its Top-K.  The averages and the pillars are computed
-// exactly as the standalone selection computes them.
+// descriptors.  CTAs take published averaging items before attention units (before
+// draft units only, in launches with more than 16 rows per kv head).  The last
+// averaging item of a head to finish runs its Top-K.  The averages and the pillars are computed exactly as the
+// standalone selection computes them.
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // bound of every wait: 2 s
 
@@ -232,20 +232,28 @@ __device__ bool sel_request_ok(const AttnParams& p, int r, const Req& q, int* K,
 }
 
 // Next task of the CTA (thread 0): 2 = averaging item (queue slot in *item), 1 =
-// attention unit (*item), 0 = nothing left.  A CTA claims an averaging slot with an
-// atomic add when one looks published, and keeps that claim (*pending) while it takes
-// attention units until the slot's descriptor has been written; with no attention left
-// it waits for its own slot (bounded, with backoff), so waiting CTAs poll distinct
-// addresses.
-__device__ int next_task(const AttnParams& p, long long total, uint32_t total_avg, bool& attn_left,
-                         long long& pending, uint32_t* item) {
+// attention unit (*item), 0 = nothing left.  A CTA prefers a published averaging item
+// to an attention unit; with VERIFY_FIRST it takes none until every verification unit
+// has been claimed.  Launches with more than 16 query rows per kv head verify in long
+// units (about 120 us each at 40 rows): averaging items taken between them stretched
+// the verification phase and the selection of the last heads ended the launch (Qwen3-
+// 14B shape, 128 requests: 0.571 ms verification first against 0.594 ms), while the
+// 16-row bench launch is 0.9 % shorter with the averaging interleaved (measured on
+// GB300).  A CTA claims an averaging slot with an atomic add when one looks published,
+// and keeps that claim (*pending) while it takes attention units until the slot's
+// descriptor has been written; with no attention left it waits for its own slot
+// (bounded, with backoff), so waiting CTAs poll distinct addresses.
+template <bool VERIFY_FIRST>
+__device__ int next_task(const AttnParams& p, long long total, long long n_verify, uint32_t total_avg,
+                         bool& attn_left, long long& pending, uint32_t* item) {
   const bool sel = total_avg > 0;
   unsigned long long t0 = 0;
   unsigned sleep_ns = 64;
   for (;;) {
     if (sel) {
       if (pending < 0 && pending != -2 &&
-          (!attn_left || ld_volatile(p.avg_head) < ld_volatile(p.avg_reserve))) {
+          (!attn_left || ((!VERIFY_FIRST || (long long)ld_volatile(p.q_next) >= n_verify) &&
+                          ld_volatile(p.avg_head) < ld_volatile(p.avg_reserve)))) {
         const uint32_t c = atomicAdd(p.avg_head, 1u);
         pending = c < total_avg ? (long long)c : -2;   // -2: every item is claimed
       }
@@ -579,7 +587,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     __syncthreads();
     if (tid == 0) {
       uint32_t item = 0;
-      s_misc[3] = next_task(p, total, total_avg, attn_left, pending, &item);
+      s_misc[3] = next_task<(MT > 1)>(p, total, n_verify, total_avg, attn_left, pending, &item);
       s_misc[0] = int(item);
       s_misc[2] = 0;
     }
