@@ -115,6 +115,8 @@ struct Smem {
   static constexpr int off_rl = off_rmax + kRed;
   static constexpr int off_prefix = off_rl + kRedL;
   static size_t bytes(int batch) { return off_prefix + size_t(batch + 1) * 4; }
+  // merge_partials' weights and row statistics fit from the start of the ring to the row ids
+  static_assert(off_rows >= (kMaxChunks * SSPEC_MAX_ROWS + 2 * SSPEC_MAX_ROWS) * 4, "merge scratch");
 };
 
 // byte offset of 16-byte chunk `ch` of row `row` in a 256-byte-row swizzled tile
@@ -132,20 +134,44 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch) {
 }
 
 // Merge the nch partial states of one (request, kv head).  `scratch` is free shared
-// memory (the K/V ring) large enough for nch * rows weights plus 2 * rows floats.
+// memory (the K/V ring and what follows it, up to the row ids) of `scratch_floats`
+// floats, at least nch * rows weights plus 2 * rows floats.  The partial states were
+// just written by other CTAs (L2); the loads are issued in batches so that a merge
+// costs a few L2 round trips.  Each output accumulates its chunks in chunk order and
+// each row sum in the same lane order whatever the batching.
 template <int MT, int W>
 __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long long u0, int nch,
-                               float* scratch) {
+                               float* scratch, int scratch_floats) {
+  constexpr int NT = W * 32;
   const size_t ustride = size_t(p.unit_stride);
   const float* base = p.partials + size_t(u0) * ustride;
+  const float* m_base = base + size_t(p.rows_max) * kHeadDim;         // running maxima (log2 units)
+  const float* l_base = base + size_t(p.rows_max) * (kHeadDim + 1);   // row sums
   const int G = p.group, rows = q.rows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float* sw = scratch;                       // [nch][rows] weights
-  float* s_inv = scratch + nch * rows;       // [rows] 1 / sum
+  const int n = nch * rows;
+  float* sw = scratch;                       // [nch][rows] maxima, then weights
+  float* s_inv = scratch + n;                // [rows] 1 / sum
   float* s_lse = s_inv + rows;               // [rows]
-  for (int e = tid; e < nch * rows; e += W * 32) {
-    const int c = e / rows, row = e - c * rows;
-    sw[e] = __ldcg(base + c * ustride + size_t(p.rows_max) * kHeadDim + row);
+  float* sl = s_lse + rows;                  // [nch][rows] row sums, when they fit
+  const bool l_smem = 2 * n + 2 * rows <= scratch_floats;
+  for (int e0 = tid; e0 < n; e0 += 8 * NT) {
+    float m[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + i * NT;
+      const int c = e / rows, row = e - c * rows;
+      m[i] = e < n ? __ldcg(m_base + c * ustride + row) : 0.f;
+      l[i] = l_smem && e < n ? __ldcg(l_base + c * ustride + row) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + i * NT;
+      if (e < n) {
+        sw[e] = m[i];
+        if (l_smem) sl[e] = l[i];
+      }
+    }
   }
   __syncthreads();
   for (int row = warp; row < rows; row += W) {
@@ -156,7 +182,7 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
     float ls = 0.f;
     for (int c = lane; c < nch; c += 32) {
       const float w = exp2f(sw[c * rows + row] - M);
-      ls += w * __ldcg(base + c * ustride + size_t(p.rows_max) * (kHeadDim + 1) + row);
+      ls += w * (l_smem ? sl[c * rows + row] : __ldcg(l_base + c * ustride + row));
       sw[c * rows + row] = w;
     }
 #pragma unroll
@@ -167,35 +193,61 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
     }
   }
   __syncthreads();
-  for (int e = tid; e < rows * (kHeadDim / 4); e += W * 32) {
-    const int row = e / (kHeadDim / 4);
-    const int d = (e % (kHeadDim / 4)) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* src = base + row * kHeadDim + d;
+  // outputs: kE float4 columns a thread at a time, 4 chunks each (4 kE loads in flight;
+  // 4 columns on the 128-thread kernel, 2 on the wider ones: measured on GB300)
+  constexpr int kE = NT <= 128 ? 4 : 2, kC = 4;
+  const int ne = rows * (kHeadDim / 4);
+  for (int e0 = tid; e0 < ne; e0 += kE * NT) {
+    float4 acc[kE];
+    const float* src[kE];
+    int rowk[kE];
+#pragma unroll
+    for (int k = 0; k < kE; ++k) {
+      const int e = min(e0 + k * NT, ne - 1);
+      rowk[k] = e / (kHeadDim / 4);
+      src[k] = base + rowk[k] * kHeadDim + (e % (kHeadDim / 4)) * 4;
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     int c = 0;
-    for (; c + 4 <= nch; c += 4) {
-      float4 v[4];
+    for (; c + kC <= nch; c += kC) {
+      float4 v[kE][kC];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = __ldcg(reinterpret_cast<const float4*>(src + (c + i) * ustride));
+      for (int k = 0; k < kE; ++k)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float w = sw[(c + i) * rows + row];
-        acc.x += w * v[i].x; acc.y += w * v[i].y; acc.z += w * v[i].z; acc.w += w * v[i].w;
-      }
+        for (int i = 0; i < kC; ++i) v[k][i] = __ldcg(reinterpret_cast<const float4*>(src[k] + (c + i) * ustride));
+#pragma unroll
+      for (int k = 0; k < kE; ++k)
+#pragma unroll
+        for (int i = 0; i < kC; ++i) {
+          const float w = sw[(c + i) * rows + rowk[k]];
+          acc[k].x += w * v[k][i].x; acc[k].y += w * v[k][i].y; acc[k].z += w * v[k][i].z; acc[k].w += w * v[k][i].w;
+        }
     }
     for (; c < nch; ++c) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + c * ustride));
-      const float w = sw[c * rows + row];
-      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+      float4 v[kE];
+#pragma unroll
+      for (int k = 0; k < kE; ++k) v[k] = __ldcg(reinterpret_cast<const float4*>(src[k] + c * ustride));
+#pragma unroll
+      for (int k = 0; k < kE; ++k) {
+        const float w = sw[c * rows + rowk[k]];
+        acc[k].x += w * v[k].x; acc[k].y += w * v[k].y; acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
+      }
     }
-    const float inv = s_inv[row];
-    const long long orow = q.verify ? q.qbase + row / G : q.qbase;
-    const int hq = h * G + (q.verify ? row % G : row);
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(p.out + (size_t(orow) * p.hq + hq) * kHeadDim + d) = pk;
-    if (d == 0) p.lse[size_t(orow) * p.hq + hq] = s_lse[row];
+#pragma unroll
+    for (int k = 0; k < kE; ++k) {
+      const int e = e0 + k * NT;
+      if (e < ne) {
+        const int row = rowk[k], d = (e % (kHeadDim / 4)) * 4;
+        const float inv = s_inv[row];
+        const long long orow = q.verify ? q.qbase + row / G : q.qbase;
+        const int hq = h * G + (q.verify ? row % G : row);
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+        pk.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+        *reinterpret_cast<uint2*>(p.out + (size_t(orow) * p.hq + hq) * kHeadDim + d) = pk;
+        if (d == 0) p.lse[size_t(orow) * p.hq + hq] = s_lse[row];
+      }
+    }
   }
 }
 
@@ -993,7 +1045,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       __syncthreads();
       if (s_misc[1]) {
         __threadfence();
-        merge_partials<MT, W>(p, q, h, slot - c, nch, reinterpret_cast<float*>(smem + S::off_k));
+        merge_partials<MT, W>(p, q, h, slot - c, nch, reinterpret_cast<float*>(smem + S::off_k), S::off_rows / 4);
         if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
         if (total_avg > 0 && q.verify) {
           int K;
