@@ -428,9 +428,9 @@ __device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t
     const long long ibase = p.idx_off[r];
     const long long istride = (p.idx_off[r + 1] - ibase) / p.hkv;
     const sel::TopkSmem sm{s_hist, s_gt, s_eq, s_pos, s_key, s_misc, s_warp, kCand};
-    // ballot words per warp per round of the candidate pass: 16 on the 128-thread
-    // kernel, 32 on the wider ones (measured on GB300)
-    sel::topk_ascending<NT, NT <= 128 ? 16 : 32, true>(S, L, K, ghist, p.sel_idx + ibase + h * istride, sm);
+    // quads of keys a lane loads per round of the candidate pass: 8 (4 on the
+    // 256-thread kernel, whose registers are capped at 128)
+    sel::topk_ascending<NT, NT <= 192 ? 8 : 4, true>(S, L, K, ghist, p.sel_idx + ibase + h * istride, sm);
     if (tid == 0) {
       p.sel_nsel[r] = K;
       p.sel_cnt[size_t(r) * p.hkv + h] = 0;

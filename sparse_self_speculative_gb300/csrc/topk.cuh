@@ -20,7 +20,6 @@
 namespace sspec {
 namespace sel {
 
-constexpr int kWords = 8;       // ballot words a warp builds per round of loads
 constexpr float kLog2eAvg = 1.4426950408889634f;   // log2(e)
 
 // Shared memory handed to the Top-K routines.
@@ -155,63 +154,107 @@ __device__ void find_digit(const uint32_t* s_hist, int nbins, int kr, int* s_war
 }
 
 // Top-K when the keys whose top digit is at least d1 (the digit of the K-th largest
-// key) number at most sm.cap: one pass over U collects their positions in position
-// order, the two lower digits are found among their keys in shared memory, and the
-// result is filtered out of that ordered list.  kr is the rank of the K-th largest
+// key) number at most sm.cap: one pass over U collects their positions and keys in
+// position order, the two lower digits are found among the keys in shared memory, and
+// the result is filtered out of that ordered list.  kr is the rank of the K-th largest
 // key among the keys whose top digit is d1.
-template <int NT, int KW>
+//
+// The candidate pass reads U through its 16-byte-aligned view A (A = U - mis, mis the
+// word offset of U in its 16-byte line): a lane loads the 4 keys of one aligned quad at
+// a time (the partial quads at either end key by key, so no address leaves U), KQ quads
+// a round, the warps' quads of a round consecutive.  Ballots give each candidate its rank
+// inside its warp's run; one block scan a round of the warps' counts places the runs.
+template <int NT, int KQ>
 __device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int kr, int ncand, int32_t* out,
                                      const TopkSmem& sm) {
+  constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // Ballot words ("top digit >= d1" bits of 32 positions) of up to sm.cap words at a
-  // time go to the key array, free until the keys are gathered; one block scan then
-  // gives each thread the output offset of its contiguous run of words.
-  uint32_t* words = sm.key;
-  const int seg_pos = sm.cap * 32;
+  const unsigned lt = lanemask_lt();
+  const int mis = int((reinterpret_cast<uintptr_t>(U) >> 2) & 3u);
+  const uint32_t* A = U - mis;
+  const int La = L + mis;                             // aligned positions a = position + mis
+  int* s_cnt = reinterpret_cast<int*>(sm.gt);        // per-warp counts, two rounds alternating
   int run = 0;
-  for (int seg0 = 0; seg0 < L; seg0 += seg_pos) {
-    const int nwords = (min(seg_pos, L - seg0) + 31) / 32;
-    for (int w0 = warp * KW; w0 < nwords; w0 += (NT / 32) * KW) {
-      uint32_t u[KW];
+  int par = 0;
+  for (int r0 = 0; r0 < La; r0 += NW * KQ * 128, par ^= 1) {
+    // The 512-thread selection kernel (64 registers) records which keys lie in U while
+    // loading; the attention kernels recompute it (they schedule better so: measured).
+    constexpr bool kInAtLoad = NT >= 512;
+    uint32_t v[KQ][4];
+    unsigned in[KQ];   // bit j: aligned position a0 + j lies in U
 #pragma unroll
-      for (int i = 0; i < KW; ++i) {
-        const int t = seg0 + (w0 + i) * 32 + lane;
-        u[i] = (w0 + i < nwords && t < L) ? __ldcg(U + t) : 0u;
-      }
+    for (int q = 0; q < KQ; ++q) {
+      const int a0 = r0 + (warp * KQ + q) * 128 + 4 * lane;
+      if (a0 >= mis && a0 + 4 <= La) {
+        const uint4 x = __ldcg(reinterpret_cast<const uint4*>(A + a0));
+        v[q][0] = x.x;
+        v[q][1] = x.y;
+        v[q][2] = x.z;
+        v[q][3] = x.w;
+        in[q] = 15u;
+      } else {
+        in[q] = 0u;
 #pragma unroll
-      for (int i = 0; i < KW; ++i) {
-        const int t = seg0 + (w0 + i) * 32 + lane;
-        const unsigned m = __ballot_sync(0xffffffffu, w0 + i < nwords && t < L && (u[i] >> 21) >= d1);
-        if (lane == 0 && w0 + i < nwords) words[w0 + i] = m;
-      }
-    }
-    __syncthreads();
-    const int wpt = (nwords + NT - 1) / NT;
-    const int a0 = min(nwords, tid * wpt), a1 = min(nwords, a0 + wpt);
-    int c = 0;
-    for (int w = a0; w < a1; ++w) c += __popc(words[w]);
-    int tot;
-    int at = run + block_exclusive_scan<NT>(c, sm.warp, &tot);
-    for (int w = a0; w < a1; ++w) {
-      uint32_t wb = words[w];
-      while (wb) {
-        const int bit = __ffs(wb) - 1;
-        if (at < sm.cap) sm.pos[at] = seg0 + w * 32 + bit;
-        ++at;
-        wb &= wb - 1u;
+        for (int j = 0; j < 4; ++j) {
+          const bool ok = a0 + j >= mis && a0 + j < La;
+          v[q][j] = ok ? __ldcg(A + a0 + j) : 0u;
+          in[q] |= unsigned(ok) << j;
+        }
       }
     }
-    run += tot;
+    // flags[q] bit j: aligned position a0 + j lies in U and its key's top digit is >= d1;
+    // off[q]: candidates of this warp's run before this lane's quad q
+    unsigned flags[KQ];
+    int off[KQ];
+    int wtot = 0;
+#pragma unroll
+    for (int q = 0; q < KQ; ++q) {
+      unsigned f = 0u;
+      if constexpr (kInAtLoad) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f |= unsigned((v[q][j] >> 21) >= d1) << j;
+        f &= in[q];
+      } else {
+        const int a0 = r0 + (warp * KQ + q) * 128 + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          f |= unsigned(a0 + j >= mis && a0 + j < La && (v[q][j] >> 21) >= d1) << j;
+      }
+      flags[q] = f;
+      int before = 0, tot = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const unsigned bj = __ballot_sync(0xffffffffu, (f >> j) & 1u);
+        before += __popc(bj & lt);
+        tot += __popc(bj);
+      }
+      off[q] = wtot + before;
+      wtot += tot;
+    }
+    if (lane == 0) s_cnt[par * NW + warp] = wtot;
     __syncthreads();
-  }
-  // their keys (U is resident in L2)
-  for (int i0 = tid; i0 < ncand; i0 += NT * 4) {
-    uint32_t u[4];
+    int base = run, total = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) u[i] = i0 + i * NT < ncand ? __ldcg(U + sm.pos[i0 + i * NT]) : 0u;
+    for (int w = 0; w < NW; ++w) {
+      const int c = s_cnt[par * NW + w];
+      base += w < warp ? c : 0;
+      total += c;
+    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (i0 + i * NT < ncand) sm.key[i0 + i * NT] = u[i];
+    for (int q = 0; q < KQ; ++q) {
+      int at = base + off[q];
+      const int p0 = r0 + (warp * KQ + q) * 128 + 4 * lane - mis;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((flags[q] >> j) & 1u) {
+          if (at < sm.cap) {
+            sm.pos[at] = p0 + j;
+            sm.key[at] = v[q][j];
+          }
+          ++at;
+        }
+    }
+    run += total;
   }
   __syncthreads();
   // digits 2 (bits 20..10) and 3 (bits 9..0) of the K-th largest key
@@ -259,11 +302,11 @@ __device__ void topk_from_candidates(const uint32_t* U, int L, uint32_t d1, int 
 
 // Top-K of S[0..L) (fp32, >= 0) into out[0..K), ascending by position; equal keys go
 // to the lower position.  `ghist` holds the histogram of the top 11 bits of all L keys;
-// it is read and cleared here.  KW ballot words per warp are loaded at a time in the
-// candidate pass (registers against round trips; the result does not depend on it).
-// PREFETCH first asks L2 for all of S (for averages written long enough ago, by other
-// CTAs, to have left it).
-template <int NT, int KW = kWords, bool PREFETCH = false>
+// it is read and cleared here.  A lane loads KQ quads of keys a round in the candidate
+// pass (registers against round trips; the result does not depend on it).  PREFETCH
+// first asks L2 for all of S (for averages written long enough ago, by other CTAs, to
+// have left it).
+template <int NT, int KQ = 2, bool PREFETCH = false>
 __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, int32_t* out, const TopkSmem& sm) {
   constexpr int kSeg = NT * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -293,7 +336,7 @@ __device__ void topk_ascending(const float* S, int L, int K, uint32_t* ghist, in
   const int ncand = sm.misc[1] + int(sm.hist[sm.misc[0]]);   // keys with top digit >= the K-th's
   __syncthreads();
   if (ncand <= sm.cap) {
-    topk_from_candidates<NT, KW>(U, L, prefix >> 21, kr, ncand, out, sm);
+    topk_from_candidates<NT, KQ>(U, L, prefix >> 21, kr, ncand, out, sm);
     return;
   }
   // digits 2 (bits 20..10) and 3 (bits 9..0) by two more passes over S
