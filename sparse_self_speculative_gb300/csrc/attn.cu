@@ -709,47 +709,41 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     // ---- 1. row ids (page * Hkv + h) * 16 + slot: one per 16-token page of a
     // verification chunk (its positions are contiguous and start on a page), one per
     // entry of a draft chunk ----
-    // A thread takes entries tid, tid + kThreads, ... (at most kIds of them); all their
-    // pillar-list loads are issued together, then all their block-table loads, so the
-    // unit's set-up waits for two rounds of loads however many entries a thread has.
+    // A thread takes entries tid, tid + kThreads, ... two at a time: both pillar-list
+    // loads are issued together, then both block-table loads.
     const int nids = q.verify ? (ntok + kPage - 1) / kPage : ntok;
-    constexpr int kIds = (kChunk + kThreads - 1) / kThreads;
-    static_assert(kVerifyChunkMax / kPage <= kChunk, "a verification unit has at most kChunk row ids");
-    int pos[kIds], bad[kIds];
+    const int32_t* idx_row = p.idx + (q.verify ? 0 : q.idx_base + h * q.idx_stride);
+    const int* bt_row = p.block_table + size_t(r) * p.max_pages;
+#pragma unroll 1
+    for (int i0 = tid; i0 < nids; i0 += 2 * kThreads) {
+      int pos[2], pg[2], bad[2];
 #pragma unroll
-    for (int j = 0; j < kIds; ++j) {
-      const int i = tid + j * kThreads;
-      const int e = q.verify ? tok0 + i * kPage : tok0 + i;
-      pos[j] = 0;
-      bad[j] = 0;
-      if (i < nids) {
-        if (q.verify) pos[j] = e;
-        else if (e < q.nsel) pos[j] = p.idx[q.idx_base + h * q.idx_stride + e];
-        else pos[j] = q.sel_len + (e - q.nsel);
+      for (int j = 0; j < 2; ++j) {
+        const int i = i0 + j * kThreads;
+        const int e = q.verify ? tok0 + i * kPage : tok0 + i;
+        pos[j] = q.verify ? e : (e < q.nsel ? (i < nids ? idx_row[e] : 0) : q.sel_len + (e - q.nsel));
       }
-    }
-    int pg[kIds];
 #pragma unroll
-    for (int j = 0; j < kIds; ++j) {
-      const int i = tid + j * kThreads;
-      if (i < nids && !q.verify && tok0 + i < q.nsel && (pos[j] < 0 || pos[j] >= q.sel_len))
-        bad[j] = SSPEC_DEVERR_INDEX_OOB;
-      pg[j] = i < nids && !bad[j] ? p.block_table[size_t(r) * p.max_pages + (pos[j] >> 4)] : -1;
-    }
+      for (int j = 0; j < 2; ++j) {
+        const int i = i0 + j * kThreads;
+        bad[j] = !q.verify && tok0 + i < q.nsel && (pos[j] < 0 || pos[j] >= q.sel_len) ? SSPEC_DEVERR_INDEX_OOB : 0;
+        pg[j] = i < nids && !bad[j] ? bt_row[pos[j] >> 4] : -1;
+      }
 #pragma unroll
-    for (int j = 0; j < kIds; ++j) {
-      const int i = tid + j * kThreads;
-      if (i < nids) {
-        int rid = -1;
-        if (!bad[j]) {
-          if (pg[j] < 0 || pg[j] >= p.num_pages) bad[j] = SSPEC_DEVERR_PAGE_OOB;
-          else rid = (pg[j] * p.hkv + h) * kPage + (pos[j] & (kPage - 1));
+      for (int j = 0; j < 2; ++j) {
+        const int i = i0 + j * kThreads;
+        if (i < nids) {
+          int rid = -1;
+          if (!bad[j]) {
+            if (pg[j] < 0 || pg[j] >= p.num_pages) bad[j] = SSPEC_DEVERR_PAGE_OOB;
+            else rid = (pg[j] * p.hkv + h) * kPage + (pos[j] & (kPage - 1));
+          }
+          if (bad[j]) {
+            atomicOr(p.err, bad[j]);
+            s_misc[2] = 1;
+          }
+          s_row[i] = rid;
         }
-        if (bad[j]) {
-          atomicOr(p.err, bad[j]);
-          s_misc[2] = 1;
-        }
-        s_row[i] = rid;
       }
     }
 
