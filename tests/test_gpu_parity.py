@@ -320,6 +320,29 @@ def test_fused_step_and_select_parity(hq, hkv, lens):
     assert np.mean(overlaps) > 0.98
 
 
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (40, 8)])
+def test_fused_select_on_short_and_odd_lengths(hq, hkv):
+    """The Top-K candidate pass reads a head's averages as 16-byte quads of their
+    16-byte-aligned view, key by key in the partial quads at either end.  Lengths 8 to
+    11 and 37 to 40 put the heads' averages at every offset inside a 16-byte line (and a
+    head of 8 to 11 keys has partial quads at both ends); 4,099 and 4,101 span several
+    rounds of the pass.  One template per shape: 16, 32 and 40 query rows per kv head."""
+    k, s = 8, 0.05
+    lens = [8, 9, 10, 11, 37, 38, 39, 40, 4099, 4101, 300]
+    wl = synth.make_workload("odd", 4242 + hq, hq, hkv, lens, plant="kv_per_head", plant_frac=0.02)
+    dkv = hz.DeviceKV(wl, fill="device")
+    buckets = [0] * (len(lens) - 1) + [3]    # every request verifies but the last
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, pillars="synthetic")
+    S = st.score_buffer()
+    st.fused_select(S)
+    torch.cuda.synchronize()
+    assert hz.device_error(st.ws) == 0
+    vr = np.flatnonzero(st.is_verify)
+    assert len(vr) == len(lens) - 1
+    for r in vr:
+        _select_check(st, int(r), S)
+
+
 def test_fused_equals_separate_launches_bitwise():
     """The fused launch computes each unit exactly as the single-template launches do."""
     import sparse_self_speculative_gb300 as ss
