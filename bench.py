@@ -206,7 +206,7 @@ def step_accounting(st):
     row_bytes = hkv * 128 * 2 * 2                              # K and V of one token, all KV heads
     kv_verify = int((L[v] * row_bytes).sum())
     kv_draft = int(((nsel[~v] + steps[~v] + 1) * row_bytes).sum())
-    logit_bytes = int((L[v] * hkv * st.k * G * 4).sum())
+    logit_bytes = int((L[v] * hkv * st.k * G * st.d_logits.element_size()).sum())   # fp32 or bf16 dump
     q_rows = int(st.q_off[-1])
     io_bytes = q_rows * hq * 128 * 2 * 2 + q_rows * hq * 4      # q in, out, lse
     idx_bytes = int((nsel[~v] * hkv * 4).sum())
@@ -248,7 +248,9 @@ def run_ours(args, world, rank, local):
     wl = synth.named_workload(name, seed, seq_lens=lens)
     buckets, _ = ss.sspec_assign_buckets(k, [0] * (k + 1), B)
     dkv = hz.DeviceKV(wl, fill="device")
-    st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="setup")
+    dump_bf16 = args.dump == "bf16"
+    st = hz.UnifiedStep(wl, dkv, k, s, buckets, verify_bucket=0, pillars="setup",
+                        logit_dtype=ss.SSPEC_LOGITS_BF16 if dump_bf16 else ss.SSPEC_LOGITS_F32)
     acc = step_accounting(st)
     stream = torch.cuda.current_stream()
     S = st.score_buffer()
@@ -420,7 +422,9 @@ def run_ours(args, world, rank, local):
     # dump, the selection, queries, outputs and indices are reported beside them.
     kbytes = acc["fused_bytes"] + (acc["select_bytes"] if fused_sel else 0)
     all_gbs = kbytes / (f_ms / 1e3) / 1e9
-    ratio = _traffic_ratio(fused_sel)
+    # the traffic capture was taken with the fp32 dump
+    ratio = None if dump_bf16 else _traffic_ratio(fused_sel)
+    attn_ratio = None if dump_bf16 else _traffic_ratio(False)
     traffic = None if ratio is None else kbytes * ratio
     kv_gbs = acc["kv_bytes"] / (f_ms / 1e3) / 1e9
     total_gbs = acc["fused_bytes"] / (f_ms / 1e3) / 1e9
@@ -433,7 +437,8 @@ def run_ours(args, world, rank, local):
                                f"{acc['n_verify']} verify + {acc['n_draft']} draft requests",
                    "global_batch": B * world, "parallelism": f"replicas{world}",
                    "l2": f"inputs larger than L2 ({(acc['fused_bytes'] + acc['select_bytes']) / 1e9:.2f} GB read "
-                         f"or written per step vs 129 MB of L2; no flush)"},
+                         f"or written per step vs 129 MB of L2; no flush)",
+                   "logit_dump": "bf16 (optional)" if dump_bf16 else "fp32"},
         "kv_gbs": kv_gbs,
         "selection": "inside the fused launch" if fused_sel else "separate launch",
         "fused_ms": f_ms, "select_ms": None if fused_sel else statistics.mean(select_ms),
@@ -446,7 +451,8 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": kv_gbs, "peak": peak, "unit": "GB/s", "frac": kv_gbs / peak,
                      "traffic": traffic,
                      "traffic_note": (TRAFFIC_CAPTURE["capture"] + "; DRAM bytes of all the launch's traffic")
-                     if traffic is not None else "null: no ncu capture taken on the current kernel sources",
+                     if traffic is not None else ("null: the ncu capture is of the fp32 dump" if dump_bf16 else
+                                                  "null: no ncu capture taken on the current kernel sources"),
                      "kernel": "attn_persistent (fused step" + (" with selection)" if fused_sel else ")"),
                      "algorithmic_bytes": acc["kv_bytes"],
                      "algorithmic": "K and V bytes, every row read once (verify: all L rows; draft: K + j + 1 rows)",
@@ -461,7 +467,7 @@ def run_ours(args, world, rank, local):
             "kernel": "attn_persistent (fused step without selection)", "ms": attn_only_ms,
             "achieved": acc["fused_bytes"] / (attn_only_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
             "frac": acc["fused_bytes"] / (attn_only_ms / 1e3) / 1e9 / peak,
-            "traffic": None if _traffic_ratio(False) is None else acc["fused_bytes"] * _traffic_ratio(False)},
+            "traffic": None if attn_ratio is None else acc["fused_bytes"] * attn_ratio},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host buffers, one stream per direction, two device buffer sets: step "
                           "t+1 in and step t-1 out while step t's kernel runs"},
@@ -1264,6 +1270,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-offload", action="store_true", help="skip the KV offload / reload context timing")
     ap.add_argument("--batch", type=int, default=0, help="first N requests of the workload (profiling cases)")
+    ap.add_argument("--dump", default="fp32", choices=["fp32", "bf16"],
+                    help="element type of the logit dump (bf16: the optional half-size dump; context only)")
     ap.add_argument("--select", default="fused", choices=["fused", "separate"],
                     help="pillar selection inside the fused launch, or as its own launch after it")
     ap.add_argument("--graph", action="store_true",

@@ -79,12 +79,22 @@ enum {
    draft step.  A longer request is skipped and reported with SSPEC_DEVERR_LENGTH. */
 #define SSPEC_MAX_TOKENS 196608
 
+/* Element type of the logit dump (sspec_shape.logit_dtype).  SSPEC_LOGITS_BF16 stores
+   each scaled logit rounded to the nearest bf16 (ties to even; -inf stays -inf), half
+   the dump's bytes written and read back (SparseSpec's optional bf16 dump); the
+   selection then averages the rounded logits.  Outputs and LSE do not depend on it. */
+#define SSPEC_LOGITS_F32 0
+#define SSPEC_LOGITS_BF16 1   /* the dump buffer must start on a 4-byte boundary (else
+                                 SSPEC_ERR_INVALID_ARG) and span a multiple of 4 bytes: the
+                                 selection reads bf16 logits as halves of aligned words */
+
 typedef struct {
   int32_t num_q_heads;   /* Hq */
   int32_t num_kv_heads;  /* Hkv, Hq % Hkv == 0 */
   int32_t head_dim;      /* must be 128 */
   int32_t page_size;     /* must be 16 */
   float sm_scale;        /* usually 1/sqrt(128) */
+  int32_t logit_dtype;   /* SSPEC_LOGITS_F32 (0) or SSPEC_LOGITS_BF16 */
 } sspec_shape;
 
 typedef struct {
@@ -118,7 +128,8 @@ size_t sspec_workspace_size(const sspec_shape* shape, int32_t batch, int32_t nq,
  *   seq_lens  device int32 [batch], nq <= seq_len <= 16 * max_pages_per_req
  *   out       device bf16 [batch][nq][Hq][128]
  *   lse       device fp32 [batch][nq][Hq]
- *   logits    device fp32, nullable (no dump).  Request r's dump starts at
+ *   logits    device fp32 (bf16 when shape->logit_dtype is SSPEC_LOGITS_BF16),
+ *             nullable (no dump).  Request r's dump starts at
  *             element logit_off[r] and is laid out [Hkv][nq*G][seq_len],
  *             row j*G+g holding query j of head h*G+g; masked entries are -inf.
  *             logit_off[r+1] - logit_off[r] must be >= Hkv*nq*G*seq_len.
@@ -126,7 +137,7 @@ size_t sspec_workspace_size(const sspec_shape* shape, int32_t batch, int32_t nq,
  */
 int sspec_verify_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
                       int32_t nq, const void* q, const int32_t* seq_lens, void* out,
-                      float* lse, float* logits, const int64_t* logit_off, void* workspace,
+                      float* lse, void* logits, const int64_t* logit_off, void* workspace,
                       size_t ws_bytes, sspec_stream_t stream);
 
 /*
@@ -141,7 +152,8 @@ int sspec_verify_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_
  *   S[h][t] = (1/(nq*G)) * sum_{j<nq, g<G} exp(logit[h][j*G+g][t] - lse[j][h*G+g])
  *   idx of head h = the K positions with the largest S[h][.], equal scores
  *   going to the lower position, written ascending.
- *   logits, logit_off  as written by sspec_verify_attn / sspec_fused_step;
+ *   logits, logit_off  as written by sspec_verify_attn / sspec_fused_step
+ *                      (element type shape->logit_dtype);
  *                      logit_off[r] must be a multiple of nq*G.
  *   lse        device fp32, row (q_off ? q_off[r] : r*nq) + j of width Hq
  *   q_off      device int64 [batch+1] or null
@@ -152,7 +164,7 @@ int sspec_verify_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_
  *   nsel       device int32 [batch]: K of each processed request.
  */
 int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, float s,
-                         const float* logits, const int64_t* logit_off, const float* lse,
+                         const void* logits, const int64_t* logit_off, const float* lse,
                          const int64_t* q_off, const int32_t* seq_lens, float* avg_scores,
                          int32_t* idx, const int64_t* idx_off, int32_t* nsel, void* workspace,
                          size_t ws_bytes, sspec_stream_t stream);
@@ -226,14 +238,14 @@ int sspec_sparse_draft_attn_noalloc(const sspec_shape* shape, const sspec_paged_
  *   q_off     device int64 [batch+1]
  *   out       device bf16 [rows][Hq][128];  lse  device fp32 [rows][Hq]
  *   logits / logit_off  dump of the verifying requests (drafts may have
- *             empty ranges); logits nullable
+ *             empty ranges; elements of shape->logit_dtype); logits nullable
  *   sel_lens, idx, idx_off, nsel  read for drafting requests only
  */
 int sspec_fused_step(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch,
                      int32_t k, const int32_t* bucket, int32_t verify_bucket, const void* q,
                      const int64_t* q_off, const int32_t* seq_lens, const int32_t* sel_lens,
                      const int32_t* idx, const int64_t* idx_off, const int32_t* nsel, void* out,
-                     float* lse, float* logits, const int64_t* logit_off, void* workspace,
+                     float* lse, void* logits, const int64_t* logit_off, void* workspace,
                      size_t ws_bytes, sspec_stream_t stream);
 
 /*
@@ -264,7 +276,7 @@ int sspec_fused_step_select(const sspec_shape* shape, const sspec_paged_kv* kv, 
                             int32_t k, const int32_t* bucket, int32_t verify_bucket, const void* q,
                             const int64_t* q_off, const int32_t* seq_lens, const int32_t* sel_lens,
                             int32_t* idx, const int64_t* idx_off, int32_t* nsel, float s,
-                            float* avg_scores, void* out, float* lse, float* logits,
+                            float* avg_scores, void* out, float* lse, void* logits,
                             const int64_t* logit_off, void* workspace, size_t ws_bytes,
                             sspec_stream_t stream);
 

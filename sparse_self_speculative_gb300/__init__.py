@@ -31,12 +31,14 @@ SSPEC_DEVERR_TIMEOUT = 32
 SSPEC_MAX_BATCH = 1024
 SSPEC_MAX_ROWS = 64
 SSPEC_MAX_TOKENS = 196608
+SSPEC_LOGITS_F32 = 0        # element type of the logit dump (sspec_shape.logit_dtype)
+SSPEC_LOGITS_BF16 = 1
 
 
 class SspecShape(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("sm_scale", ctypes.c_float)]
+                ("sm_scale", ctypes.c_float), ("logit_dtype", ctypes.c_int32)]
 
 
 class SspecPagedKV(ctypes.Structure):
@@ -145,8 +147,11 @@ def _check(fn, rc):
         raise SspecError(fn, rc)
 
 
-def make_shape(num_q_heads: int, num_kv_heads: int, sm_scale: float | None = None) -> SspecShape:
-    return SspecShape(num_q_heads, num_kv_heads, 128, 16, (128 ** -0.5) if sm_scale is None else sm_scale)
+def make_shape(num_q_heads: int, num_kv_heads: int, sm_scale: float | None = None,
+               logit_dtype: int = 0) -> SspecShape:
+    """Shape of a model's attention; logit_dtype SSPEC_LOGITS_BF16 selects the bf16 dump."""
+    return SspecShape(num_q_heads, num_kv_heads, 128, 16, (128 ** -0.5) if sm_scale is None else sm_scale,
+                      logit_dtype)
 
 
 def make_kv(k_cache, v_cache, block_table) -> SspecPagedKV:

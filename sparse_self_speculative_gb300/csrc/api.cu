@@ -26,6 +26,7 @@ int check_shape(const sspec_shape* s) {
     return SSPEC_ERR_INVALID_ARG;
   if (s->num_q_heads > 256 || s->num_kv_heads > 64) return SSPEC_ERR_UNSUPPORTED_SHAPE;
   if (!(s->sm_scale > 0.f) || !std::isfinite(s->sm_scale)) return SSPEC_ERR_INVALID_ARG;
+  if (s->logit_dtype != SSPEC_LOGITS_F32 && s->logit_dtype != SSPEC_LOGITS_BF16) return SSPEC_ERR_INVALID_ARG;
   return SSPEC_OK;
 }
 
@@ -79,7 +80,7 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
                   int mode, const int32_t* bucket, int32_t verify_bucket, const void* q,
                   const int64_t* q_off, const int32_t* seq_lens, const int32_t* sel_lens,
                   const int32_t* idx, const int64_t* idx_off, const int32_t* nsel, void* out,
-                  float* lse, float* logits, const int64_t* logit_off, void* workspace,
+                  float* lse, void* logits, const int64_t* logit_off, void* workspace,
                   size_t ws_bytes, sspec_stream_t stream, float sel_s = 0.f, float* sel_scores = nullptr,
                   int32_t* sel_idx = nullptr, int32_t* sel_nsel = nullptr, PreLaunch pre = PreLaunch{}) {
   int rc = check_shape(shape);
@@ -95,6 +96,7 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
     if (nq < 1) return SSPEC_ERR_INVALID_ARG;
     if (nq * G > SSPEC_MAX_ROWS) return SSPEC_ERR_UNSUPPORTED_SHAPE;
     if (logits && !logit_off) return SSPEC_ERR_INVALID_ARG;
+    if (logits && shape->logit_dtype == SSPEC_LOGITS_BF16 && !aligned(logits, 4)) return SSPEC_ERR_INVALID_ARG;
   }
   if (any_draft && (!sel_lens || !idx || !idx_off || !nsel)) return SSPEC_ERR_INVALID_ARG;
   if (mode == kByBucket && (!bucket || !q_off)) return SSPEC_ERR_INVALID_ARG;
@@ -129,6 +131,7 @@ int run_attention(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t ba
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.logits = any_verify ? logits : nullptr;
+  p.logit_bf16 = shape->logit_dtype == SSPEC_LOGITS_BF16;
   p.logit_off = logit_off;
   p.err = w.err;
   p.q_next = &w.hdr->attn_next;
@@ -185,7 +188,7 @@ size_t sspec_workspace_size(const sspec_shape* shape, int32_t batch, int32_t nq,
 }
 
 int sspec_verify_attn(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch, int32_t nq,
-                      const void* q, const int32_t* seq_lens, void* out, float* lse, float* logits,
+                      const void* q, const int32_t* seq_lens, void* out, float* lse, void* logits,
                       const int64_t* logit_off, void* workspace, size_t ws_bytes, sspec_stream_t stream) {
   return run_attention(shape, kv, batch, nq, kAllVerify, nullptr, 0, q, nullptr, seq_lens, nullptr,
                        nullptr, nullptr, nullptr, out, lse, logits, logit_off, workspace, ws_bytes, stream);
@@ -202,7 +205,7 @@ int sspec_sparse_draft_attn(const sspec_shape* shape, const sspec_paged_kv* kv, 
 int sspec_fused_step(const sspec_shape* shape, const sspec_paged_kv* kv, int32_t batch, int32_t k,
                      const int32_t* bucket, int32_t verify_bucket, const void* q, const int64_t* q_off,
                      const int32_t* seq_lens, const int32_t* sel_lens, const int32_t* idx,
-                     const int64_t* idx_off, const int32_t* nsel, void* out, float* lse, float* logits,
+                     const int64_t* idx_off, const int32_t* nsel, void* out, float* lse, void* logits,
                      const int64_t* logit_off, void* workspace, size_t ws_bytes, sspec_stream_t stream) {
   if (k < 1 || verify_bucket < 0 || verify_bucket > k) return SSPEC_ERR_INVALID_ARG;
   return run_attention(shape, kv, batch, k, kByBucket, bucket, verify_bucket, q, q_off, seq_lens, sel_lens,
@@ -213,7 +216,7 @@ int sspec_fused_step_select(const sspec_shape* shape, const sspec_paged_kv* kv, 
                             const int32_t* bucket, int32_t verify_bucket, const void* q, const int64_t* q_off,
                             const int32_t* seq_lens, const int32_t* sel_lens, int32_t* idx,
                             const int64_t* idx_off, int32_t* nsel, float s, float* avg_scores, void* out,
-                            float* lse, float* logits, const int64_t* logit_off, void* workspace,
+                            float* lse, void* logits, const int64_t* logit_off, void* workspace,
                             size_t ws_bytes, sspec_stream_t stream) {
   if (k < 1 || verify_bucket < 0 || verify_bucket > k) return SSPEC_ERR_INVALID_ARG;
   if (!(s > 0.f && s <= 1.f) || !avg_scores || !logits || !logit_off || !idx || !idx_off || !nsel)
@@ -223,7 +226,7 @@ int sspec_fused_step_select(const sspec_shape* shape, const sspec_paged_kv* kv, 
                        idx, nsel);
 }
 
-int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, float s, const float* logits,
+int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, float s, const void* logits,
                          const int64_t* logit_off, const float* lse, const int64_t* q_off,
                          const int32_t* seq_lens, float* avg_scores, int32_t* idx, const int64_t* idx_off,
                          int32_t* nsel, void* workspace, size_t ws_bytes, sspec_stream_t stream) {
@@ -232,6 +235,7 @@ int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, fl
   if (batch < 0 || batch > SSPEC_MAX_BATCH || nq < 1) return SSPEC_ERR_INVALID_ARG;
   if (!(s > 0.f && s <= 1.f)) return SSPEC_ERR_INVALID_ARG;
   if (!logits || !logit_off || !lse || !seq_lens || !idx || !idx_off || !nsel) return SSPEC_ERR_INVALID_ARG;
+  if (shape->logit_dtype == SSPEC_LOGITS_BF16 && !aligned(logits, 4)) return SSPEC_ERR_INVALID_ARG;
   const int G = shape->num_q_heads / shape->num_kv_heads;
   if (nq * G > SSPEC_MAX_ROWS) return SSPEC_ERR_UNSUPPORTED_SHAPE;
   Ws w;
@@ -245,6 +249,7 @@ int sspec_select_pillars(const sspec_shape* shape, int32_t batch, int32_t nq, fl
   p.group = G;
   p.s = s;
   p.logits = logits;
+  p.logit_bf16 = shape->logit_dtype == SSPEC_LOGITS_BF16;
   p.logit_off = logit_off;
   p.lse = lse;
   p.q_off = q_off;

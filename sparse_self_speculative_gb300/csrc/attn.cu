@@ -359,7 +359,7 @@ __device__ void publish_avg(const AttnParams& p, int r, int h, int L, int passes
 // verifying (request, kv head) from the logit dump and LSE, adds their first radix digit
 // to the head's histogram; the head's last item runs its Top-K.  `ring` is the CTA's
 // K/V staging ring (64 KB, idle between units).
-template <int NT>
+template <int NT, typename LT>
 __device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t* ring, int* s_misc, int* s_warp) {
   const int kBlk = NT * kAvgPass * passes;
   constexpr int kCand = 6144;
@@ -393,7 +393,7 @@ __device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t
   sel_request_ok(p, r, q, &K, false);
   const int G = p.group, L = q.L, rows = q.rows;
   const int nb = (L + kBlk - 1) / kBlk;
-  const float* lg = p.logits + q.loff + size_t(h) * rows * L;
+  const LT* lg = static_cast<const LT*>(p.logits) + q.loff + size_t(h) * rows * L;
   const int t_end = min(L, (b + 1) * kBlk);
   constexpr int kStep = NT * kAvgPass;
   // the registers hold one pass of loads; L2 prefetches keep the next passes in flight
@@ -441,7 +441,9 @@ __device__ void avg_item(const AttnParams& p, uint32_t slot, int passes, uint8_t
 // Register caps: 4-warp CTAs fit 3 per SM (170 registers), wider ones 2.
 constexpr int attn_min_blocks(int warps) { return warps <= 4 ? 3 : 2; }
 
-template <int MT, int WN>
+// LT: element type of the logit dump (float, or uint16_t holding bf16 bits), fixed at
+// compile time so the fp32 path carries no branch for the other.
+template <int MT, int WN, typename LT>
 __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_persistent(const AttnParams p) {
   constexpr int W = MT * WN;                 // warps: WN per 16-row query tile
   constexpr int kThreads = W * 32;
@@ -647,7 +649,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
     const int kind = s_misc[3];
     if (kind == 0) break;
     if (kind == 2) {
-      avg_item<kThreads>(p, uint32_t(s_misc[0]), avg_passes, smem + S::off_k, s_misc, s_warp);
+      avg_item<kThreads, LT>(p, uint32_t(s_misc[0]), avg_passes, smem + S::off_k, s_misc, s_warp);
       continue;
     }
     const long long u = s_misc[0];   // unit index over all phases
@@ -820,7 +822,7 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) vis_lim[hh] = q.verify ? q.L - p.nq + (mg * 16 + g8 + hh * 8) / G : INT_MAX;
     // the unit's first logit of row 0 of this kv head in the dump
-    float* dump_base = dump ? p.logits + q.loff + size_t(h) * q.rows * q.L + tok0 : nullptr;
+    LT* dump_base = dump ? static_cast<LT*>(p.logits) + q.loff + size_t(h) * q.rows * q.L + tok0 : nullptr;
 
     for (int t = 0; t < ntiles; ++t) {
       cp_async_wait<kStages - 2>();
@@ -963,11 +965,11 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       if (dump) {
         const int cols = min(kTile, ntok - t * kTile);
         for (int row = warp; row < q.rows; row += W) {
-          float* dst = dump_base + size_t(row) * q.L + t * kTile;
+          LT* dst = dump_base + size_t(row) * q.L + t * kTile;
 #pragma unroll
           for (int c0 = 0; c0 < kTile; c0 += 32) {
             const int col = c0 + lane;
-            if (col < cols) dst[col] = ld_shared_f32(kb + dump_stage_off(row, col));
+            if (col < cols) put_logit(dst + col, ld_shared_f32(kb + dump_stage_off(row, col)));
           }
         }
       }
@@ -1082,15 +1084,15 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
   }
 }
 
-template <int MT, int WN>
+template <int MT, int WN, typename LT>
 cudaError_t launch_mt(const AttnParams& p, cudaStream_t stream) {
   constexpr int W = MT * WN;
   const size_t smem = Smem<MT, W>::bytes(p.batch);
-  cudaError_t e = cudaFuncSetAttribute(attn_persistent<MT, WN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_persistent<MT, WN, LT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Smem<MT, W>::bytes(SSPEC_MAX_BATCH)));
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_persistent<MT, WN>, W * 32, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_persistent<MT, WN, LT>, W * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // Every CTA of the persistent grid takes tasks until none is left, so a small batch
@@ -1103,21 +1105,26 @@ cudaError_t launch_mt(const AttnParams& p, cudaStream_t stream) {
                              (p.sel_scores ? (16LL * p.max_pages + W * 32 * kAvgPass - 1) / (W * 32 * kAvgPass) : 0);
   const long long tasks = (long long)p.batch * p.hkv * per_head;
   const int grid = int(tasks < q.grid_full ? (tasks > 0 ? tasks : 1) : q.grid_full);
-  attn_persistent<MT, WN><<<grid, W * 32, smem, stream>>>(q);
+  attn_persistent<MT, WN, LT><<<grid, W * 32, smem, stream>>>(q);
   return cudaGetLastError();
+}
+
+template <typename LT>
+cudaError_t launch_rows(const AttnParams& p, cudaStream_t stream) {
+  const int mt = (p.rows_max + 15) / 16;
+  switch (mt) {
+    case 1: return launch_mt<1, 4, LT>(p, stream);
+    case 2: return launch_mt<2, 4, LT>(p, stream);
+    case 3: return launch_mt<3, 2, LT>(p, stream);
+    case 4: return launch_mt<4, 2, LT>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
-  const int mt = (p.rows_max + 15) / 16;
-  switch (mt) {
-    case 1: return launch_mt<1, 4>(p, stream);
-    case 2: return launch_mt<2, 4>(p, stream);
-    case 3: return launch_mt<3, 2>(p, stream);
-    case 4: return launch_mt<4, 2>(p, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return p.logit_bf16 ? launch_rows<uint16_t>(p, stream) : launch_rows<float>(p, stream);
 }
 
 }  // namespace sspec

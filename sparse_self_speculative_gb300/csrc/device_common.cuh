@@ -77,6 +77,15 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   return v;
 }
 
+// bf16 bits of v rounded to the nearest bf16, ties to even (infinities kept)
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// one logit of the dump: fp32 as is, bf16 rounded to nearest even
+__device__ __forceinline__ void put_logit(float* d, float v) { *d = v; }
+__device__ __forceinline__ void put_logit(uint16_t* d, float v) { *d = bf16_bits(v); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -120,7 +120,7 @@ struct AttnParams {
   const int32_t* nsel;
   uint16_t* out;
   float* lse;
-  float* logits;              // nullable
+  void* logits;               // nullable; fp32, or bf16 bits when logit_bf16
   const int64_t* logit_off;
   // workspace
   int32_t* err;
@@ -145,12 +145,14 @@ struct AttnParams {
   unsigned long long* avg_slots;   // averaging-item queue
   uint32_t* avg_reserve;
   uint32_t* avg_head;
+  int logit_bf16;             // the dump holds bf16 (selects the kernel instantiation)
 };
 
 struct SelectParams {
   int batch, nq, hq, hkv, group;
   float s;
-  const float* logits;
+  const void* logits;         // fp32, or bf16 bits when logit_bf16
+  int logit_bf16;
   const int64_t* logit_off;
   const float* lse;
   const int64_t* q_off;

@@ -131,9 +131,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_persistent(const Select
     }
     __syncthreads();
     const int t_lo = b * kSelBlock;
-    sel::average_block<kSelThreads, kSelPer, kSelRowGroup, true>(p.logits + q.loff + size_t(h) * q.rows * q.L, q.L, q.rows,
-                                                   s_lse, t_lo, min(q.L, t_lo + kSelBlock),
-                                                   p.scores + q.soff + size_t(h) * q.L, s_hist);
+    const size_t lg_off = q.loff + size_t(h) * q.rows * q.L;   // the head's first logit
+    float* S = p.scores + q.soff + size_t(h) * q.L;
+    if (p.logit_bf16)
+      sel::average_block<kSelThreads, kSelPer, kSelRowGroup, true>(static_cast<const uint16_t*>(p.logits) + lg_off, q.L,
+                                                                   q.rows, s_lse, t_lo, min(q.L, t_lo + kSelBlock), S,
+                                                                   s_hist);
+    else
+      sel::average_block<kSelThreads, kSelPer, kSelRowGroup, true>(static_cast<const float*>(p.logits) + lg_off, q.L,
+                                                                   q.rows, s_lse, t_lo, min(q.L, t_lo + kSelBlock), S,
+                                                                   s_hist);
     __syncthreads();
     for (int i = tid; i < kSelBins; i += kSelThreads) {
       const uint32_t v = s_hist[i];

@@ -34,6 +34,9 @@ struct TopkSmem {
   int cap;
 };
 
+// Value of a bf16 logit (widened exactly).
+__device__ __forceinline__ float bf16_value(uint32_t b) { return __uint_as_float(b << 16); }
+
 // Averages positions t_lo + tid + j * NT (j < PER) below t1 of one kv head:
 // S[t] = (1/rows) sum_row exp(logit[row][t] - lse[row]), rows added in order.  lg
 // points at the head's first logit row (row stride L); s_lse holds the rows' natural
@@ -42,35 +45,64 @@ struct TopkSmem {
 // first is used, so the row grouping sets the loads in flight but not the result.  The
 // top 11 bits of every average are counted in s_hist (warp-aggregated shared-memory
 // atomics).  STREAM reads the logits with an evict-first hint (they are not read again).
-template <int NT, int PER, int RG, bool STREAM>
-__device__ __forceinline__ void average_block(const float* lg, int L, int rows, const float* s_lse, int t_lo,
+// T is the dump's element type: float, or uint16_t holding bf16 bits.
+template <int NT, int PER, int RG, bool STREAM, typename T>
+__device__ __forceinline__ void average_block(const T* lg, int L, int rows, const float* s_lse, int t_lo,
                                               int t1, float* S, uint32_t* s_hist) {
   const int tid = threadIdx.x, lane = tid & 31;
   const float inv_rows = 1.f / float(rows);
-  const float* col = lg + t_lo + tid;     // this thread's first position in row 0
+  const T* col = lg + t_lo + tid;         // this thread's first position in row 0
   const int rem = t1 - t_lo - tid;        // position j * NT is valid iff below rem
   float acc[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) acc[j] = 0.f;
 #pragma unroll 1
   for (int r0 = 0; r0 < rows; r0 += RG) {
-    float v[RG][PER];
+    if constexpr (sizeof(T) == 4) {
+      float v[RG][PER];
 #pragma unroll
-    for (int i = 0; i < RG; ++i) {
-      const bool row_ok = r0 + i < rows;
-      const float* src = col + size_t(row_ok ? r0 + i : 0) * L;
+      for (int i = 0; i < RG; ++i) {
+        const bool row_ok = r0 + i < rows;
+        const T* src = col + size_t(row_ok ? r0 + i : 0) * L;
 #pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const bool ok = row_ok && j * NT < rem;
-        v[i][j] = ok ? (STREAM ? __ldcs(src + j * NT) : __ldcg(src + j * NT)) : -INFINITY;
+        for (int j = 0; j < PER; ++j) {
+          const bool ok = row_ok && j * NT < rem;
+          v[i][j] = ok ? (STREAM ? __ldcs(src + j * NT) : __ldcg(src + j * NT)) : -INFINITY;
+        }
       }
-    }
 #pragma unroll
-    for (int i = 0; i < RG; ++i) {
-      // exp(v - lse) as 2^(v log2 e - lse log2 e): one FMA and the hardware exp2
-      const float l2 = s_lse[r0 + i] * kLog2eAvg;
+      for (int i = 0; i < RG; ++i) {
+        // exp(v - lse) as 2^(v log2 e - lse log2 e): one FMA and the hardware exp2
+        const float l2 = s_lse[r0 + i] * kLog2eAvg;
 #pragma unroll
-      for (int j = 0; j < PER; ++j) acc[j] += exp2f(fmaf(v[i][j], kLog2eAvg, -l2));
+        for (int j = 0; j < PER; ++j) acc[j] += exp2f(fmaf(v[i][j], kLog2eAvg, -l2));
+      }
+    } else {
+      // bf16: each element is read as its half of the aligned 32-bit word that holds it
+      // (2-byte global loads measured about five times slower in the fused launch's
+      // averaging).  A thread's elements of one row share their half (NT is even); the
+      // word stays inside the dump, which starts on a 4-byte boundary and spans a
+      // multiple of 4 bytes.  Out-of-range positions read a pair of bf16 -inf.
+      uint32_t v[RG][PER];
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
+        const bool row_ok = r0 + i < rows;
+        const T* src = col + size_t(row_ok ? r0 + i : 0) * L;
+        const uint32_t hi = uint32_t(reinterpret_cast<uintptr_t>(src) >> 1) & 1u;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(src - hi);
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const bool ok = row_ok && j * NT < rem;
+          const uint32_t x = ok ? (STREAM ? __ldcs(w + j * NT / 2) : __ldcg(w + j * NT / 2)) : 0xFF80FF80u;
+          v[i][j] = (x >> (16 * hi)) & 0xFFFFu;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
+        const float l2 = s_lse[r0 + i] * kLog2eAvg;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) acc[j] += exp2f(fmaf(bf16_value(v[i][j]), kLog2eAvg, -l2));
+      }
     }
   }
 #pragma unroll
@@ -88,18 +120,19 @@ __device__ __forceinline__ void average_block(const float* lg, int L, int rows, 
 }
 
 // Prefetches into L2 the logit lines of positions [t0, t1) of `rows` rows (row stride
-// L, first row at lg).  Each row's range is named through its positions t0, t0 + 32,
-// ... and t1 - 1: consecutive named positions are one 128-byte line apart, and t1 - 1
-// names the last line, so every line the range spans is fetched and no address leaves
-// the range.
-template <int NT>
-__device__ __forceinline__ void prefetch_pass(const float* lg, int L, int rows, int t0, int t1) {
+// L, first row at lg).  Each row's range is named through its positions t0, t0 + E,
+// ... and t1 - 1 (E elements to a 128-byte line): consecutive named positions are one
+// line apart, and t1 - 1 names the last line, so every line the range spans is fetched
+// and no address leaves the range.
+template <int NT, typename T>
+__device__ __forceinline__ void prefetch_pass(const T* lg, int L, int rows, int t0, int t1) {
+  constexpr int E = 128 / int(sizeof(T));
   const int n = t1 - t0;
   if (n <= 0) return;
-  const int m = (n + 31) / 32 + 1;   // named positions per row
+  const int m = (n + E - 1) / E + 1;   // named positions per row
   for (int i = threadIdx.x; i < rows * m; i += NT) {
     const int row = i / m, k = i - row * m;
-    prefetch_l2(lg + size_t(row) * L + (k < m - 1 ? t0 + 32 * k : t1 - 1));
+    prefetch_l2(lg + size_t(row) * L + (k < m - 1 ? t0 + E * k : t1 - 1));
   }
 }
 

@@ -111,14 +111,15 @@ class UnifiedStep:
     """
 
     def __init__(self, wl: synth.Workload, dkv: DeviceKV, k: int, s: float, buckets, verify_bucket: int = 0,
-                 pillars: str = "synthetic", device: str = "cuda"):
+                 pillars: str = "synthetic", device: str = "cuda", logit_dtype: int = 0):
         import sparse_self_speculative_gb300 as ss
         self.wl, self.dkv, self.k, self.s = wl, dkv, k, s
         self.buckets = np.asarray(buckets, dtype=np.int32)
         self.verify_bucket = verify_bucket
         B, hq, hkv = wl.batch, wl.num_q_heads, wl.num_kv_heads
         G = hq // hkv
-        self.shape = ss.make_shape(hq, hkv)
+        self.shape = ss.make_shape(hq, hkv, logit_dtype=logit_dtype)
+        self.logit_dtype = logit_dtype
         L = wl.seq_lens.astype(np.int64)
         self.steps = np.array([draft_step(int(b), verify_bucket, k) for b in self.buckets], dtype=np.int32)
         self.is_verify = self.steps < 0
@@ -153,7 +154,12 @@ class UnifiedStep:
         self.d_bucket = torch.from_numpy(self.buckets).to(dev)
         self.d_logit_off = torch.from_numpy(self.logit_off).to(dev)
         self.d_idx_off = torch.from_numpy(self.idx_off).to(dev)
-        self.d_logits = torch.empty(max(1, int(self.logit_off[-1])), dtype=torch.float32, device=dev)
+        # the logit dump: fp32, or bf16 bits in int16 storage
+        # (a bf16 dump spans a multiple of 4 bytes: an even element count)
+        n_lg = max(1, int(self.logit_off[-1]))
+        self.d_logits = torch.empty(n_lg + (n_lg & 1) if logit_dtype == ss.SSPEC_LOGITS_BF16 else n_lg,
+                                    dtype=torch.int16 if logit_dtype == ss.SSPEC_LOGITS_BF16 else torch.float32,
+                                    device=dev)
         self.d_out = torch.empty((nrows, hq, 128), dtype=torch.int16, device=dev)
         self.d_lse = torch.empty((nrows, hq), dtype=torch.float32, device=dev)
         self.d_idx = torch.zeros(max(1, int(self.idx_off[-1])), dtype=torch.int32, device=dev)

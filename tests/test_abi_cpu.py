@@ -83,6 +83,18 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call_verify(lib, ss.SspecShape(16, 8, 128, 32, 0.1), kv) == ss.SSPEC_ERR_UNSUPPORTED_SHAPE
     assert _call_verify(lib, ss.SspecShape(16, 6, 128, 16, 0.1), kv) == ss.SSPEC_ERR_INVALID_ARG
     assert _call_verify(lib, ss.SspecShape(16, 8, 128, 16, -1.0), kv) == ss.SSPEC_ERR_INVALID_ARG
+    # the dump's element type is fp32 or bf16, nothing else
+    assert _call_verify(lib, ss.SspecShape(16, 8, 128, 16, 0.1, 2), kv) == ss.SSPEC_ERR_INVALID_ARG
+    assert _call_verify(lib, ss.SspecShape(16, 8, 128, 16, 0.1, -1), kv) == ss.SSPEC_ERR_INVALID_ARG
+    assert lib.sspec_workspace_size(ctypes.byref(ss.SspecShape(16, 8, 128, 16, 0.1, 2)), 4, 8, 1000) == 0
+    # a bf16 dump starts on a 4-byte boundary (the selection reads it as aligned words):
+    # the same call fails on the tiny workspace once the dump is aligned
+    b16 = ss.make_shape(16, 8, logit_dtype=ss.SSPEC_LOGITS_BF16)
+    assert _call_verify(lib, b16, kv, logits=4098, loff=16, ws_bytes=16) == ss.SSPEC_ERR_INVALID_ARG
+    assert _call_verify(lib, b16, kv, logits=4100, loff=16, ws_bytes=16) == ss.SSPEC_ERR_WORKSPACE_TOO_SMALL
+    assert _call_verify(lib, shape, kv, logits=4098, loff=16, ws_bytes=16) == ss.SSPEC_ERR_WORKSPACE_TOO_SMALL
+    assert lib.sspec_workspace_size(ctypes.byref(ss.make_shape(16, 8, logit_dtype=ss.SSPEC_LOGITS_BF16)), 4, 8,
+                                    1000) == lib.sspec_workspace_size(ctypes.byref(shape), 4, 8, 1000)
     assert _call_verify(lib, shape, kv, batch=-1) == ss.SSPEC_ERR_INVALID_ARG
     assert _call_verify(lib, shape, kv, batch=ss.SSPEC_MAX_BATCH + 1) == ss.SSPEC_ERR_INVALID_ARG
     assert _call_verify(lib, shape, kv, nq=0) == ss.SSPEC_ERR_INVALID_ARG
@@ -243,10 +255,10 @@ def test_reference_arm_json_line_has_the_contract_keys():
 
 
 def test_attention_templates_do_not_spill():
-    """The attention templates stay within their register budgets (a spill in the
-    per-tile loop costs several percent on the GB300: one was caught this way).  Compiled
-    here for sm_103a with ptxas's resource report; the 64-row template, which no
-    benchmark workload uses, is allowed its few spilled bytes."""
+    """The attention templates, for both dump element types, stay within their register
+    budgets (a spill in the per-tile loop costs several percent on the GB300: one was
+    caught this way).  Compiled here for sm_103a with ptxas's resource report; the
+    64-row template, which no benchmark workload uses, is allowed its spilled bytes."""
     import re
     import subprocess
     from sparse_self_speculative_gb300 import _build
@@ -257,13 +269,13 @@ def test_attention_templates_do_not_spill():
     report = {}
     current = None
     for line in res.stderr.splitlines():
-        m = re.search(r"Compiling entry function '.*attn_persistentILi(\d)ELi(\d)E", line)
+        m = re.search(r"Compiling entry function '.*attn_persistentILi(\d)ELi(\d)E(\w)", line)
         if m:
-            current = (int(m.group(1)), int(m.group(2)))
+            current = (int(m.group(1)), int(m.group(2)), m.group(3))   # f: fp32 dump, t: bf16 bits
         m = re.search(r"(\d+) bytes spill stores", line)
         if m and current is not None:
             report[current] = int(m.group(1))
             current = None
-    assert set(report) == {(1, 4), (2, 4), (3, 2), (4, 2)}, report
+    assert set(report) == {(mt, wn, t) for mt, wn in ((1, 4), (2, 4), (3, 2), (4, 2)) for t in "ft"}, report
     for key, spill in report.items():
-        assert spill == 0 or key == (4, 2), (key, spill)
+        assert spill == 0 or key[:2] == (4, 2), (key, spill)
