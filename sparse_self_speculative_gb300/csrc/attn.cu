@@ -194,8 +194,8 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
   }
   __syncthreads();
   // outputs: kE float4 columns a thread at a time, 4 chunks each (4 kE loads in flight;
-  // 4 columns on the 128-thread kernel, 2 on the wider ones: measured on GB300)
-  constexpr int kE = NT <= 128 ? 4 : 2, kC = 4;
+  // 2 columns on the 192-thread kernel, 4 on the others: measured on GB300)
+  constexpr int kE = NT == 192 ? 2 : 4, kC = 4;
   const int ne = rows * (kHeadDim / 4);
   for (int e0 = tid; e0 < ne; e0 += kE * NT) {
     float4 acc[kE];
