@@ -442,6 +442,19 @@ int64_t sspec_kv_fifo_pending(const sspec_kv_fifo* fifo);
  */
 int sspec_get_device_error(const void* workspace, int32_t* out, int32_t clear, sspec_stream_t stream);
 
+/*
+ * Read-only streaming probe of device memory, for measurement only (not a step of
+ * the method): reads `bytes` of `buf` once, front to back, with 16-byte loads from
+ * every SM, and writes the XOR of all the buffer's 32-bit words to *sink.  Timing
+ * it with events on `stream` gives the read-only HBM rate that the attention's K/V
+ * rate is set against beside a copy's (a copy also writes).
+ *   buf    device memory, 16-byte aligned; bytes > 0 and a multiple of 16
+ *   sink   device uint32, 4-byte aligned; cleared on `stream`, then written
+ * Returns SSPEC_ERR_INVALID_ARG for null or misaligned pointers or a bad size
+ * (nothing enqueued), SSPEC_ERR_CUDA if CUDA refuses the clear or the launch.
+ */
+int sspec_hbm_read_probe(const void* buf, size_t bytes, uint32_t* sink, sspec_stream_t stream);
+
 /* Static English text of an SSPEC_* return code. */
 const char* sspec_error_string(int code);
 

@@ -84,6 +84,7 @@ _SIGS = {
     "sspec_kv_offload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, ctypes.c_size_t, _P, _P]),
     "sspec_kv_reload": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, ctypes.c_size_t, _P, _P]),
     "sspec_get_device_error": (ctypes.c_int, [_P, _P, _I32, _P]),
+    "sspec_hbm_read_probe": (ctypes.c_int, [_P, ctypes.c_size_t, _P, _P]),
     "sspec_kv_fifo_create": (_P, []),
     "sspec_kv_fifo_destroy": (None, [_P]),
     "sspec_kv_fifo_push": (ctypes.c_int, [_P, _I32, _I32]),
@@ -249,6 +250,15 @@ def sspec_get_device_error(workspace, out, clear: bool = False, stream=None) -> 
     _check("sspec_get_device_error", rc)
 
 
+def sspec_hbm_read_probe(buf, sink, nbytes=None, stream=None) -> None:
+    """Reads ``nbytes`` (default: all) of the device tensor ``buf`` once and writes the
+    XOR of its 32-bit words to ``sink`` (a device int32/uint32 tensor of one element):
+    the read-only streaming probe that measurement times beside the attention."""
+    n = _nbytes(buf) if nbytes is None else int(nbytes)
+    rc = lib().sspec_hbm_read_probe(_ptr(buf), n, _ptr(sink), _stream(stream))
+    _check("sspec_hbm_read_probe", rc)
+
+
 def sspec_kv_fifo_create() -> int:
     h = lib().sspec_kv_fifo_create()
     if not h:
@@ -338,7 +348,8 @@ __all__ = [
     "sspec_workspace_size", "sspec_verify_attn", "sspec_select_pillars", "sspec_sparse_draft_attn",
     "sspec_fused_step", "sspec_fused_step_select", "sspec_sparse_draft_attn_noalloc", "sspec_assign_buckets",
     "sspec_kv_offload", "sspec_kv_reload", "sspec_kv_fifo_create", "sspec_kv_fifo_destroy", "sspec_kv_fifo_push",
-    "sspec_kv_fifo_next", "sspec_kv_fifo_pending", "sspec_get_device_error", "header_functions",
+    "sspec_kv_fifo_next", "sspec_kv_fifo_pending", "sspec_get_device_error", "sspec_hbm_read_probe",
+    "header_functions",
     "SspecStepMeta", "SspecStepCounts", "sspec_pipeline_create", "sspec_pipeline_destroy", "sspec_pipeline_admit",
     "sspec_pipeline_leave", "sspec_pipeline_relabel", "sspec_pipeline_report", "sspec_pipeline_build",
 ]

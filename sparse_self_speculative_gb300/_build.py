@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libsspec.so")
-SOURCES = ["api.cu", "attn.cu", "select.cu", "noalloc.cu", "kvcopy.cu", "pipeline.cu"]
+SOURCES = ["api.cu", "attn.cu", "select.cu", "noalloc.cu", "kvcopy.cu", "pipeline.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -138,10 +138,15 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch) {
 // floats, at least nch * rows weights plus 2 * rows floats.  The partial states were
 // just written by other CTAs (L2); the loads are issued in batches so that a merge
 // costs a few L2 round trips.  Each output accumulates its chunks in chunk order and
-// each row sum in the same lane order whatever the batching.
+// each row sum in the same lane order whatever the batching.  With `publish` set (a
+// verifying head whose pillars the launch selects) the head's averaging items go on
+// their queue as soon as the LSE is written, before the outputs are merged.
+template <int NT>
+__device__ void publish_avg(const AttnParams& p, int r, int h, int L, int passes);
+
 template <int MT, int W>
-__device__ void merge_partials(const AttnParams& p, const Req& q, int h, long long u0, int nch,
-                               float* scratch, int scratch_floats) {
+__device__ void merge_partials(const AttnParams& p, const Req& q, int r, int h, long long u0, int nch,
+                               float* scratch, int scratch_floats, bool publish, int avg_passes) {
   constexpr int NT = W * 32;
   const size_t ustride = size_t(p.unit_stride);
   const float* base = p.partials + size_t(u0) * ustride;
@@ -193,6 +198,13 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
     }
   }
   __syncthreads();
+  if (publish) {
+    // the LSE is final: write it and publish the head's averaging items (they read the
+    // dump and the LSE, not the outputs), so that the selection starts while the
+    // outputs are merged
+    for (int row = tid; row < rows; row += NT) p.lse[size_t(q.qbase + row / G) * p.hq + h * G + row % G] = s_lse[row];
+    publish_avg<NT>(p, r, h, q.L, avg_passes);
+  }
   // outputs: kE float4 columns a thread at a time, 4 chunks each (4 kE loads in flight;
   // 2 columns on the 192-thread kernel, 4 on the others: measured on GB300)
   constexpr int kE = NT == 192 ? 2 : 4, kC = 4;
@@ -245,7 +257,7 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
         pk.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
         pk.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
         *reinterpret_cast<uint2*>(p.out + (size_t(orow) * p.hq + hq) * kHeadDim + d) = pk;
-        if (d == 0) p.lse[size_t(orow) * p.hq + hq] = s_lse[row];
+        if (d == 0 && !publish) p.lse[size_t(orow) * p.hq + hq] = s_lse[row];
       }
     }
   }
@@ -253,8 +265,8 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int h, long lo
 
 // ---- pillar selection inside the fused step ----------------------------------------
 //
-// When the last chunk of a verifying (request, kv head) completes (its output and LSE
-// are final), that CTA publishes the head's averaging items on a second queue: slots
+// When the last chunk of a verifying (request, kv head) completes (its LSE is final),
+// that CTA publishes the head's averaging items on a second queue: slots
 // are reserved with an atomic counter and then filled with (request, head, block)
 // descriptors.  CTAs take published averaging items before attention units (before
 // draft units only, in launches with more than 16 rows per kv head).  The last
@@ -340,8 +352,8 @@ __device__ int next_task(const AttnParams& p, long long total, long long n_verif
   }
 }
 
-// Publishes the averaging items of (r, h) once its output and LSE are written (all
-// threads call it).
+// Publishes the averaging items of (r, h) once its LSE is written (all threads call
+// it).
 template <int NT>
 __device__ void publish_avg(const AttnParams& p, int r, int h, int L, int passes) {
   __threadfence();
@@ -1059,12 +1071,17 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       __syncthreads();
       if (s_misc[1]) {
         __threadfence();
-        merge_partials<MT, W>(p, q, h, slot - c, nch, reinterpret_cast<float*>(smem + S::off_k), S::off_rows / 4);
+        // the 16- and 32-row templates publish the head's averaging items from inside the
+        // merge, as soon as the LSE is final; the 48-row template, whose averaging waits
+        // for the last verification unit to be claimed anyway, after it (measured on GB300)
+        constexpr bool kEarlyPublish = MT < 3;
+        int K;
+        const bool publish = total_avg > 0 && q.verify && (kEarlyPublish ? sel_request_ok(p, r, q, &K, false) : true);
+        merge_partials<MT, W>(p, q, r, h, slot - c, nch, reinterpret_cast<float*>(smem + S::off_k), S::off_rows / 4,
+                              kEarlyPublish && publish, avg_passes);
         if (tid == 0) p.merge_cnt[size_t(r) * p.hkv + h] = 0;
-        if (total_avg > 0 && q.verify) {
-          int K;
-          if (sel_request_ok(p, r, q, &K, false)) publish_avg<kThreads>(p, r, h, q.L, avg_passes);
-        }
+        if (!kEarlyPublish && publish && sel_request_ok(p, r, q, &K, false))
+          publish_avg<kThreads>(p, r, h, q.L, avg_passes);
       }
     }
   }

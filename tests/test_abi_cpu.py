@@ -187,6 +187,18 @@ def test_device_error_accessor_host_validation(lib):
     assert fn(264, 4096, 1, None) == ss.SSPEC_ERR_INVALID_ARG     # workspaces are 256-byte aligned
 
 
+def test_read_probe_host_validation(lib):
+    """sspec_hbm_read_probe rejects null or misaligned pointers and sizes that are not
+    a positive multiple of 16 bytes before enqueuing anything."""
+    fn = lib.sspec_hbm_read_probe
+    assert fn(None, 4096, 4096, None) == ss.SSPEC_ERR_INVALID_ARG
+    assert fn(4096, 4096, None, None) == ss.SSPEC_ERR_INVALID_ARG
+    assert fn(4096, 0, 8192, None) == ss.SSPEC_ERR_INVALID_ARG
+    assert fn(4096, 4104, 8192, None) == ss.SSPEC_ERR_INVALID_ARG      # not a multiple of 16
+    assert fn(4104, 4096, 8192, None) == ss.SSPEC_ERR_INVALID_ARG      # buffer not 16-byte aligned
+    assert fn(4096, 4096, 8194, None) == ss.SSPEC_ERR_INVALID_ARG      # sink not 4-byte aligned
+
+
 def test_kv_fifo_matches_oracle_and_rejects_bad_arguments(lib):
     rng = np.random.default_rng(31)
     for _ in range(40):
