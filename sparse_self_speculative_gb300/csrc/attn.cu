@@ -297,16 +297,23 @@ __device__ bool sel_request_ok(const AttnParams& p, int r, const Req& q, int* K,
 
 // Next task of the CTA (thread 0): 2 = averaging item (queue slot in *item), 1 =
 // attention unit (*item), 0 = nothing left.  A CTA prefers a published averaging item
-// to an attention unit; with VERIFY_FIRST it takes none until every verification unit
-// has been claimed.  Launches with more than 16 query rows per kv head verify in long
-// units (about 120 us each at 40 rows): averaging items taken between them stretched
-// the verification phase and the selection of the last heads ended the launch (Qwen3-
-// 14B shape, 128 requests: 0.571 ms verification first against 0.594 ms), while the
-// 16-row bench launch is 0.9 % shorter with the averaging interleaved (measured on
-// GB300).  A CTA claims an averaging slot with an atomic add when one looks published,
+// to an attention unit; with VERIFY_FIRST only every kAvgEarlyDiv-th CTA takes one
+// before every verification unit has been claimed.  Launches with more than 16 query
+// rows per kv head verify in long units (about 120 us each at 40 rows) and are bound
+// by instruction issue, not HBM: averaging items taken by every CTA between them
+// stretched the verification phase and the selection of the last heads ended the
+// launch (Qwen3-14B shape, 128 requests: 0.594 ms against 0.571 ms with none taken
+// until the verification units are claimed), while a quarter of the CTAs reading the
+// dump back during verification uses HBM bandwidth the verification leaves idle
+// (0.5649 against 0.5713 ms; half of them 0.596 ms, a third 0.576 ms, a fifth or a
+// sixth within 0.2 % of a quarter, an eighth 0.5668 ms).  The 16-row bench launch is
+// 0.9 % shorter with the averaging interleaved on every CTA (measured on GB300).  A
+// CTA claims an averaging slot with an atomic add when one looks published,
 // and keeps that claim (*pending) while it takes attention units until the slot's
 // descriptor has been written; with no attention left it waits for its own slot
 // (bounded, with backoff), so waiting CTAs poll distinct addresses.
+constexpr int kAvgEarlyDiv = 4;
+
 template <bool VERIFY_FIRST>
 __device__ int next_task(const AttnParams& p, long long total, long long n_verify, uint32_t total_avg,
                          bool& attn_left, long long& pending, uint32_t* item) {
@@ -316,8 +323,9 @@ __device__ int next_task(const AttnParams& p, long long total, long long n_verif
   for (;;) {
     if (sel) {
       if (pending < 0 && pending != -2 &&
-          (!attn_left || ((!VERIFY_FIRST || (long long)ld_volatile(p.q_next) >= n_verify) &&
-                          ld_volatile(p.avg_head) < ld_volatile(p.avg_reserve)))) {
+          (!attn_left ||
+           ((!VERIFY_FIRST || blockIdx.x % kAvgEarlyDiv == 0 || (long long)ld_volatile(p.q_next) >= n_verify) &&
+            ld_volatile(p.avg_head) < ld_volatile(p.avg_reserve)))) {
         const uint32_t c = atomicAdd(p.avg_head, 1u);
         pending = c < total_avg ? (long long)c : -2;   // -2: every item is claimed
       }
