@@ -53,7 +53,7 @@ def source_sha() -> str:
 # multi-pass capture).  The bench line scales it to the full launch and reports it only
 # while the kernel sources are the ones the capture was taken on.
 TRAFFIC_CAPTURE = {
-    "source_sha256_prefix": "f9d7d48281ddae71",
+    "source_sha256_prefix": "8644a4694fe3b91e",
     "ratio_with_selection": 0.970,
     "ratio_attention_only": 0.988,
     "capture": "ncu --set full, one launch of the 48-request case each (dram__bytes_read.sum + "

@@ -268,10 +268,11 @@ __device__ void merge_partials(const AttnParams& p, const Req& q, int r, int h, 
 // When the last chunk of a verifying (request, kv head) completes (its LSE is final),
 // that CTA publishes the head's averaging items on a second queue: slots
 // are reserved with an atomic counter and then filled with (request, head, block)
-// descriptors.  CTAs take published averaging items before attention units (before
-// draft units only, in launches with more than 16 rows per kv head).  The last
-// averaging item of a head to finish runs its Top-K.  The averages and the pillars are computed exactly as the
-// standalone selection computes them.
+// descriptors.  CTAs take published averaging items before attention units (in
+// launches with more than 16 rows per kv head, only every fourth CTA before the last
+// verification unit is claimed).  The last averaging item of a head to finish runs its
+// Top-K.  The averages and the pillars are computed exactly as the standalone selection
+// computes them.
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // bound of every wait: 2 s
 
