@@ -53,9 +53,9 @@ def source_sha() -> str:
 # multi-pass capture).  The bench line scales it to the full launch and reports it only
 # while the kernel sources are the ones the capture was taken on.
 TRAFFIC_CAPTURE = {
-    "source_sha256_prefix": "8644a4694fe3b91e",
+    "source_sha256_prefix": "ef036f455837f961",
     "ratio_with_selection": 0.970,
-    "ratio_attention_only": 0.988,
+    "ratio_attention_only": 0.989,
     "capture": "ncu --set full, one launch of the 48-request case each (dram__bytes_read.sum + "
                "dram__bytes_write.sum; profiles/attn_persistent_qwen3_1p7b_b48.md), scaled to this launch's "
                "algorithmic bytes",

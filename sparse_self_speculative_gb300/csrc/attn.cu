@@ -858,6 +858,8 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
       const uint32_t vb = sV + st * kTile * kRowBytes;
 
       float sacc[NT][4];
+      float rmax[2] = {-INFINITY, -INFINITY};
+      bool over = false;
       if (active) {
         // ---- S = Q K^T for this warp's row tile and 8 * NT tokens ----
 #pragma unroll
@@ -882,7 +884,6 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
 
         // ---- mask: scaled logits (natural units, -inf where not visible) and the
         // per-row maximum over this warp's tokens ----
-        float rmax[2] = {-INFINITY, -INFINITY};
         // a tile whose 64 entries all exist and are visible to every row needs no mask
         const bool interior = unit_clean && (t + 1) * kTile <= ntok && tok0 + (t + 1) * kTile - 1 <= vis_all;
         if (interior) {
@@ -913,14 +914,24 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
           }
         }
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float v = rmax[hh];
-          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-          if (tq == 0) red_max[warp * 16 + g8 + hh * 8] = v * kLog2e;   // log2 units
-        }
+        for (int hh = 0; hh < 2; ++hh) over |= rmax[hh] * kLog2e > m_run[hh] + kLazyMax;
       }
-      __syncthreads();
+      // a row's reference maximum moves in this tile only if one of its logits exceeds
+      // the reference by more than kLazyMax; only then are the exact tile maxima
+      // exchanged between the row tile's warps (always on a unit's first tile)
+      const bool exchange = __syncthreads_or(over) != 0;
+      if (exchange) {
+        if (active) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float v = rmax[hh];
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+            if (tq == 0) red_max[warp * 16 + g8 + hh * 8] = v * kLog2e;   // log2 units
+          }
+        }
+        __syncthreads();
+      }
 
       if (active) {
         // ---- the logit dump is staged in this tile's K stage (free once every warp
@@ -940,21 +951,24 @@ __global__ void __launch_bounds__(MT * WN * 32, attn_min_blocks(MT * WN)) attn_p
         // by more than kLazyMax (log2 units), so probabilities stay below 2^kLazyMax and
         // most tiles need no rescale; the warp skips the rescale when no row moved
         // (the factor is then exactly 1).
-        float alpha[2], muse[2];
+        float alpha[2] = {1.f, 1.f}, muse[2];
         bool moved = false;
+        if (exchange) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r16 = g8 + hh * 8;
-          float tmax = red_max[mg * WN * 16 + r16];
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r16 = g8 + hh * 8;
+            float tmax = red_max[mg * WN * 16 + r16];
 #pragma unroll
-          for (int w = 1; w < WN; ++w) tmax = fmaxf(tmax, red_max[(mg * WN + w) * 16 + r16]);
-          const bool move = tmax > m_run[hh] + kLazyMax;
-          alpha[hh] = move ? exp2f(m_run[hh] - tmax) : 1.f;
-          m_run[hh] = move ? tmax : m_run[hh];
-          muse[hh] = (m_run[hh] == -INFINITY) ? 0.f : m_run[hh];
-          moved |= move;
+            for (int w = 1; w < WN; ++w) tmax = fmaxf(tmax, red_max[(mg * WN + w) * 16 + r16]);
+            const bool move = tmax > m_run[hh] + kLazyMax;
+            alpha[hh] = move ? exp2f(m_run[hh] - tmax) : 1.f;
+            m_run[hh] = move ? tmax : m_run[hh];
+            moved |= move;
+          }
         }
-        const bool rescale = __any_sync(0xffffffffu, moved);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) muse[hh] = (m_run[hh] == -INFINITY) ? 0.f : m_run[hh];
+        const bool rescale = exchange && __any_sync(0xffffffffu, moved);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float ls[2] = {0.f, 0.f};
