@@ -136,6 +136,78 @@ def test_verify_and_select_with_nq_queries(hq, hkv, nq, lens):
             np.testing.assert_array_equal(got, oracle.top_k_pillars(Sg[h], int(K[r])))
 
 
+def _rne_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bits of finite values rounded to nearest, ties to even (host-side input
+    preparation only; both sides then read the same bits)."""
+    u = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _lazy_moves_after_first_tile(lg: np.ndarray, tile: int = 64, lazy_log2: float = 8.0) -> int:
+    """Tiles after a row's first at which the lazily rescaled softmax must move the
+    row's reference maximum (tile maximum more than lazy_log2 above it, in log2
+    units), summed over the rows of a [rows, L] logit block read as one unit."""
+    moves = 0
+    for row in lg:
+        ref = -np.inf
+        for t0 in range(0, len(row), tile):
+            m = np.max(row[t0:t0 + tile]) * math.log2(math.e)
+            if m > ref + lazy_log2:
+                moves += t0 > 0
+                ref = m
+    return moves
+
+
+@pytest.mark.parametrize("hq,hkv,lens", [
+    (16, 8, [2500, 900]),     # 16 rows per KV head
+    (32, 8, [2100, 64]),      # 32 rows: two query tiles
+    (40, 8, [1700, 300]),     # 40 rows: three query tiles
+])
+def test_verify_with_rising_keys_moves_the_reference_inside_units(hq, hkv, lens):
+    """Keys scaled up along the sequence (x1 at the first position to x12 at the last)
+    make every row's running maximum climb past the lazy bound many times after the
+    first tile of a unit, so the tiles that exchange the row maxima between warps run
+    inside units, not only at their start; outputs, LSE and the dump still match the
+    oracle."""
+    import sparse_self_speculative_gb300 as ss
+    nq = 8
+    wl = synth.make_workload("rise", 900 + hq + len(lens), hq, hkv, lens)
+    B, G = wl.batch, hq // hkv
+    rows_k, rows_v = {}, {}
+    for r in range(B):
+        L = int(wl.seq_lens[r])
+        ramp = 1.0 + 11.0 * np.arange(L) / max(L - 1, 1)
+        rows_k[r] = _rne_bf16_bits(oracle.bf16_bits_to_f64(wl.kv_rows("k", r, np.arange(L))) * ramp[:, None, None])
+        rows_v[r] = wl.kv_rows("v", r, np.arange(L))
+    dkv = hz.DeviceKV.from_rows(wl, rows_k, rows_v)
+    q = np.stack([wl.q_rows(r, np.arange(nq)) for r in range(B)])
+    L_all = wl.seq_lens.astype(np.int64)
+    loff = np.zeros(B + 1, dtype=np.int64)
+    loff[1:] = np.cumsum(hkv * nq * G * L_all)
+    out = torch.empty((B, nq, hq, 128), dtype=torch.int16, device="cuda")
+    lse = torch.empty((B, nq, hq), dtype=torch.float32, device="cuda")
+    logits = torch.empty(int(loff[-1]), dtype=torch.float32, device="cuda")
+    shape = ss.make_shape(hq, hkv)
+    ws = hz.zero_workspace(ss.sspec_workspace_size(shape, B, nq, int(L_all.sum())))
+    ss.sspec_verify_attn(shape, dkv.kv(), B, nq, hz.bf16_i16(q).cuda(), torch.from_numpy(wl.seq_lens).cuda(), out,
+                         lse, logits, torch.from_numpy(loff).cuda(), ws)
+    torch.cuda.synchronize()
+    assert hz.device_error(ws) == 0
+    out_b, lse_h, lg_h = hz.to_bits(out), lse.cpu().numpy(), logits.cpu().numpy()
+    for r in range(B):
+        L = int(wl.seq_lens[r])
+        kf, vf = oracle.bf16_bits_to_f64(rows_k[r]), oracle.bf16_bits_to_f64(rows_v[r])
+        o_ref, l_ref, lg_ref = oracle.verify_attention(oracle.bf16_bits_to_f64(q[r]), kf, vf, hz.SCALE)
+        if L >= 1024:
+            assert _lazy_moves_after_first_tile(lg_ref.reshape(-1, L)) >= 2 * hkv * nq * G
+        hz.check_close_bf16(out_b[r], o_ref, OUT_ATOL, OUT_RTOL)
+        assert np.abs(lse_h[r] - l_ref).max() <= LSE_TOL
+        lg = lg_h[loff[r]:loff[r + 1]].reshape(hkv, nq * G, L)
+        masked = np.isneginf(lg_ref)
+        np.testing.assert_array_equal(np.isneginf(lg), masked)
+        assert np.all(np.abs(lg[~masked] - lg_ref[~masked]) <= 1e-4 + 1e-5 * np.abs(lg_ref[~masked]))
+
+
 def test_verify_page_permutation_and_causal_bit_identity():
     nq, hq, hkv = 8, 16, 8
     lens = [700, 129]
