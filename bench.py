@@ -53,7 +53,7 @@ def source_sha() -> str:
 # multi-pass capture).  The bench line scales it to the full launch and reports it only
 # while the kernel sources are the ones the capture was taken on.
 TRAFFIC_CAPTURE = {
-    "source_sha256_prefix": "ef036f455837f961",
+    "source_sha256_prefix": "bfd59ab6b6ee4b7c",
     "ratio_with_selection": 0.970,
     "ratio_attention_only": 0.989,
     "capture": "ncu --set full, one launch of the 48-request case each (dram__bytes_read.sum + "

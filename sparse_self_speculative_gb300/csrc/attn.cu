@@ -307,9 +307,10 @@ __device__ bool sel_request_ok(const AttnParams& p, int r, const Req& q, int* K,
 // until the verification units are claimed), while a quarter of the CTAs reading the
 // dump back during verification uses HBM bandwidth the verification leaves idle
 // (0.5649 against 0.5713 ms; half of them 0.596 ms, a third 0.576 ms, a fifth or a
-// sixth within 0.2 % of a quarter, an eighth 0.5668 ms).  The 16-row bench launch is
-// 0.9 % shorter with the averaging interleaved on every CTA (measured on GB300).  A
-// CTA claims an averaging slot with an atomic add when one looks published,
+// sixth within 0.2 % of a quarter, an eighth 0.5668 ms).  With 16 rows per kv head
+// (Qwen3-1.7B shape, 256 requests of lognormal lengths) the launch is 0.9 % shorter
+// with the averaging interleaved on every CTA (measured on GB300).  A CTA claims an
+// averaging slot with an atomic add when one looks published,
 // and keeps that claim (*pending) while it takes attention units until the slot's
 // descriptor has been written; with no attention left it waits for its own slot
 // (bounded, with backoff), so waiting CTAs poll distinct addresses.
